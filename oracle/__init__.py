@@ -1,0 +1,10 @@
+"""Float64 CPU oracle for exact softmax attention.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()``
+and the CPU-baseline legs of ``bench.py``; never by the library.
+"""
+from .attention import (  # noqa: F401
+    head_forward, head_probs, head_backward, forward, backward,
+    varlen_forward, varlen_backward, decode_forward, decode_partials,
+    merge_partials, split_bounds, online_head_forward,
+)

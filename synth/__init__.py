@@ -1,0 +1,151 @@
+"""Seeded synthetic inputs shared by the oracle checks, the GPU tests and the bench.
+
+This module holds only random-number generation and shape bookkeeping: no
+attention arithmetic lives here, so neither side of a parity check can borrow
+the other's maths through it.
+
+Recipe (the same for every tensor): draw fp32 values from N(0, 1) with a
+seeded ``torch.Generator`` and round them to bf16 (round to nearest even).
+Each tensor has its own seed, ``seed * 100 + idx`` with idx q=0, k=1, v=2,
+dO=3, sequence lengths=4.  The oracle consumes the very bf16 values the GPU
+kernels see (upcast to float64 on the host).
+
+Workloads (one line each, sizes as the pages' worked examples and the
+benchmark configurations state them):
+
+* ``tiny``    B=1  H=2  N=256  d=64, causal and non-causal
+* ``mid``     B=16 H=16 N=2048 d=64, non-causal
+* ``long``    B=2  H=16 N=8192 d=128, causal, K multiplied by 3 (in fp32,
+  before rounding) in heads h < H/2 so that the running maximum of the online
+  softmax jumps
+* ``varlen``  32 sequences, lengths uniform integers in [128, 4096], packed
+  end to end, H=32 d=128, causal per sequence
+* ``decode``  B=64 single queries against a 32768-token KV cache, H=32 d=128
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import Optional
+
+import torch
+
+IDX_Q, IDX_K, IDX_V, IDX_DO, IDX_LENGTHS = 0, 1, 2, 3, 4
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    kind: str                 # "dense" | "varlen" | "decode"
+    B: int                    # batch (dense/decode) or number of sequences (varlen)
+    H: int
+    N: int                    # sequence length (dense), KV cache length (decode), max length (varlen)
+    d: int
+    causal: bool
+    k_boost: float = 1.0      # multiplier on K for heads h < H/2 (1.0 = none)
+    len_lo: int = 0           # varlen: inclusive length range
+    len_hi: int = 0
+    seed: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", "dense", 1, 2, 256, 64, False),
+    "tiny_causal": Workload("tiny_causal", "dense", 1, 2, 256, 64, True),
+    "mid": Workload("mid", "dense", 16, 16, 2048, 64, False),
+    "long": Workload("long", "dense", 2, 16, 8192, 128, True, k_boost=3.0),
+    "varlen": Workload("varlen", "varlen", 32, 32, 4096, 128, True, len_lo=128, len_hi=4096),
+    "decode": Workload("decode", "decode", 64, 32, 32768, 128, False),
+}
+
+
+def _gen(seed: int, idx: int, device: str) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed * 100 + idx)
+    return g
+
+
+def randn_bf16(shape, seed: int, idx: int, device: str = "cpu",
+               head_dim_axis: Optional[int] = None, boost: float = 1.0,
+               boost_heads: int = 0) -> torch.Tensor:
+    """N(0,1) fp32 draw rounded to bf16; optionally multiply heads [0, boost_heads)
+    along ``head_dim_axis`` by ``boost`` in fp32 before the rounding."""
+    x = torch.randn(shape, generator=_gen(seed, idx, device), dtype=torch.float32, device=device)
+    if boost != 1.0 and boost_heads > 0:
+        sl = [slice(None)] * x.dim()
+        sl[head_dim_axis] = slice(0, boost_heads)
+        x[tuple(sl)] *= boost
+    return x.to(torch.bfloat16)
+
+
+def varlen_lengths(n_seqs: int, lo: int, hi: int, seed: int) -> torch.Tensor:
+    """Integer lengths drawn uniformly from [lo, hi] inclusive (int64, CPU)."""
+    return torch.randint(lo, hi + 1, (n_seqs,), generator=_gen(seed, IDX_LENGTHS, "cpu"))
+
+
+def cu_seqlens_from_lengths(lengths) -> torch.Tensor:
+    """[0, L1, L1+L2, ...] as int32 (length B+1)."""
+    lengths = torch.as_tensor(lengths, dtype=torch.int64)
+    cu = torch.zeros(lengths.numel() + 1, dtype=torch.int64)
+    cu[1:] = torch.cumsum(lengths, 0)
+    return cu.to(torch.int32)
+
+
+def make_dense(B, H, N, d, seed=0, k_boost=1.0, device="cpu", with_do=True):
+    """Q, K, V (and dO) in [B, N, H, d] bf16."""
+    shape = (B, N, H, d)
+    out = {
+        "q": randn_bf16(shape, seed, IDX_Q, device),
+        "k": randn_bf16(shape, seed, IDX_K, device, head_dim_axis=2, boost=k_boost,
+                        boost_heads=H // 2 if k_boost != 1.0 else 0),
+        "v": randn_bf16(shape, seed, IDX_V, device),
+    }
+    if with_do:
+        out["do"] = randn_bf16(shape, seed, IDX_DO, device)
+    return out
+
+
+def make_varlen(lengths, H, d, seed=0, device="cpu", with_do=True):
+    """Packed Q, K, V (and dO) in [total, H, d] bf16 plus int32 cu_seqlens."""
+    cu = cu_seqlens_from_lengths(lengths)
+    total = int(cu[-1])
+    shape = (total, H, d)
+    out = {
+        "q": randn_bf16(shape, seed, IDX_Q, device),
+        "k": randn_bf16(shape, seed, IDX_K, device),
+        "v": randn_bf16(shape, seed, IDX_V, device),
+        "cu_seqlens": cu,
+    }
+    if with_do:
+        out["do"] = randn_bf16(shape, seed, IDX_DO, device)
+    return out
+
+
+def make_decode(B, H, L, d, seed=0, device="cpu"):
+    """q [B, 1, H, d] and a KV cache [B, L, H, d] (bf16)."""
+    return {
+        "q": randn_bf16((B, 1, H, d), seed, IDX_Q, device),
+        "k": randn_bf16((B, L, H, d), seed, IDX_K, device),
+        "v": randn_bf16((B, L, H, d), seed, IDX_V, device),
+    }
+
+
+def make_workload(w: Workload, device="cpu", with_do=True):
+    if w.kind == "dense":
+        return make_dense(w.B, w.H, w.N, w.d, w.seed, w.k_boost, device, with_do)
+    if w.kind == "varlen":
+        lengths = varlen_lengths(w.B, w.len_lo, w.len_hi, w.seed)
+        out = make_varlen(lengths, w.H, w.d, w.seed, device, with_do)
+        out["lengths"] = lengths
+        return out
+    if w.kind == "decode":
+        return make_decode(w.B, w.H, w.N, w.d, w.seed, device)
+    raise ValueError(w.kind)
+
+
+def to_f64(t: torch.Tensor):
+    """Exact upcast of bf16 values to a float64 numpy array (host copy)."""
+    return t.detach().to("cpu").to(torch.float64).numpy()
