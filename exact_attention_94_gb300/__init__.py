@@ -2,15 +2,9 @@
 
 The compute runs in hand-written CUDA kernels inside ``libfa.so`` (built in
 this directory by ``build.build()``); this package only marshals arguments.
-Calls fail loudly when the library is missing: there is no fallback.
+The library is loaded on the first call, and a missing library raises: there
+is no fallback.
 """
-from . import accounting  # noqa: F401
+from . import accounting, ops  # noqa: F401
 
 __all__ = ["accounting", "ops"]
-
-
-def __getattr__(name):
-    if name == "ops":
-        from . import ops
-        return ops
-    raise AttributeError(name)

@@ -1,0 +1,209 @@
+// C ABI of the library: argument validation, tensor-map construction,
+// workspace sizing and kernel launches.  See include/fa.h for the contract of
+// every entry point.
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+namespace fa {
+
+__device__ unsigned int g_fa_error = 0;
+
+namespace {
+
+struct Options {
+  float tau = 8.0f;
+  bool poly = true;
+  unsigned long long timeout_ns = 2000000000ull;
+} g_opt;
+
+std::once_flag g_init_once;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+unsigned* g_err_ptr = nullptr;
+bool g_init_ok = false;
+
+void init_once() {
+  cudaDriverEntryPointQueryResult q;
+  void* fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+          cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  void* ep = nullptr;
+  if (cudaGetSymbolAddress(&ep, g_fa_error) == cudaSuccess) g_err_ptr = static_cast<unsigned*>(ep);
+  g_init_ok = g_encode != nullptr && g_err_ptr != nullptr;
+}
+
+bool ensure_init() {
+  std::call_once(g_init_once, init_once);
+  return g_init_ok;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool scale_ok(float s) { return std::isfinite(s) && s > 0.f; }
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+}  // namespace
+
+bool make_tmap_bhnd(CUtensorMap* m, const void* ptr, int D, int n_rows, int H, int B) {
+  const cuuint64_t e = 2;  // bytes per bf16
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)n_rows, (cuuint64_t)H, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)H * D * e, (cuuint64_t)D * e, (cuuint64_t)n_rows * H * D * e};
+  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED";
+    case FA_ERR_LAUNCH: return "FA_ERR_LAUNCH";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+  }
+  return "FA_ERR_UNKNOWN";
+}
+
+fa_status fa_set_option(fa_option opt, double value) {
+  switch (opt) {
+    case FA_OPT_RESCALE_TAU:
+      if (!(value >= 0.0 && value <= 64.0)) return FA_ERR_INVALID_ARG;
+      g_opt.tau = (float)value;
+      return FA_OK;
+    case FA_OPT_POLY_EXP:
+      g_opt.poly = value != 0.0;
+      return FA_OK;
+    case FA_OPT_WAIT_TIMEOUT_MS:
+      if (!(value >= 1.0 && value <= 600000.0)) return FA_ERR_INVALID_ARG;
+      g_opt.timeout_ns = (unsigned long long)(value * 1e6);
+      return FA_OK;
+  }
+  return FA_ERR_INVALID_ARG;
+}
+
+fa_status fa_device_error(unsigned int* code) {
+  if (!ensure_init()) return FA_ERR_LAUNCH;
+  if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_LAUNCH;
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_fa_error, sizeof(v)) != cudaSuccess) return FA_ERR_LAUNCH;
+  if (code) *code = v;
+  if (v != 0) {
+    const unsigned zero = 0;
+    cudaMemcpyToSymbol(g_fa_error, &zero, sizeof(zero));
+    return FA_ERR_TIMEOUT;
+  }
+  return FA_OK;
+}
+
+static fa_status fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu,
+                            int nbatch, int n_rows, int seq_len, int max_len, int H, int d, int causal, float scale,
+                            fa_stream_t stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (!scale_ok(scale) || (causal != 0 && causal != 1)) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_MISALIGNED;
+  if ((long long)nbatch * H > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  const int num_pairs = (max_len + 255) / 256;
+  if (num_pairs > 65535) return FA_ERR_INVALID_ARG;
+  if (!ensure_init()) return FA_ERR_LAUNCH;
+  CUtensorMap tq, tk, tv;
+  const int tb = cu ? 1 : nbatch;
+  if (!make_tmap_bhnd(&tq, q, d, n_rows, H, tb) || !make_tmap_bhnd(&tk, k, d, n_rows, H, tb) ||
+      !make_tmap_bhnd(&tv, v, d, n_rows, H, tb))
+    return FA_ERR_INVALID_ARG;
+  FwdParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.cu_seqlens = cu;
+  p.H = H;
+  p.n_rows = n_rows;
+  p.seq_len = seq_len;
+  p.num_pairs = num_pairs;
+  p.scale_log2 = scale * kLog2e;
+  p.tau = g_opt.tau;
+  p.err = g_err_ptr;
+  p.timeout_ns = g_opt.timeout_ns;
+  cudaError_t e = launch_fwd(tq, tk, tv, p, d, causal != 0, g_opt.poly, nbatch * H, (cudaStream_t)stream);
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                 int causal, float scale, fa_stream_t stream) {
+  if (B < 1 || H < 1 || N < 0) return FA_ERR_INVALID_ARG;
+  if (N == 0) return FA_OK;
+  return fwd_common(q, k, v, o, lse, nullptr, B, N, N, N, H, d, causal, scale, stream);
+}
+
+fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
+                        int num_seqs, int max_seqlen, int total_tokens, int H, int d, int causal, float scale,
+                        fa_stream_t stream) {
+  if (num_seqs < 1 || H < 1 || max_seqlen < 0 || total_tokens < 0 || !cu_seqlens) return FA_ERR_INVALID_ARG;
+  if (!aligned16(cu_seqlens) && ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0)) return FA_ERR_MISALIGNED;
+  if (total_tokens == 0 || max_seqlen == 0) return FA_OK;
+  return fwd_common(q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, 0, max_seqlen, H, d, causal, scale,
+                    stream);
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 0 || d < 1) return 0;
+  const size_t acc = (size_t)B * N * H * d * sizeof(float);
+  const size_t rows = (size_t)B * H * N * sizeof(float);
+  return ((acc + 255) & ~(size_t)255) + ((rows + 255) & ~(size_t)255);
+}
+
+size_t fa_bwd_varlen_workspace_bytes(int total_tokens, int H, int d) {
+  return fa_bwd_workspace_bytes(1, H, total_tokens, d);
+}
+
+fa_status fa_bwd(const void*, const void*, const void*, const void*, const float*, const void*, void*, void*,
+                 void*, void*, int, int, int, int, int, float, fa_stream_t) {
+  return FA_ERR_UNSUPPORTED;
+}
+
+fa_status fa_bwd_varlen(const void*, const void*, const void*, const void*, const float*, const void*, void*, void*,
+                        void*, void*, const int*, int, int, int, int, int, int, float, fa_stream_t) {
+  return FA_ERR_UNSUPPORTED;
+}
+
+size_t fa_decode_workspace_bytes(int B, int H, int d, int num_splits) {
+  if (B < 1 || H < 1 || d < 1 || num_splits < 1) return 0;
+  const size_t po = (size_t)B * H * num_splits * d * sizeof(float);
+  const size_t pl = (size_t)B * H * num_splits * sizeof(float);
+  return ((po + 255) & ~(size_t)255) + ((pl + 255) & ~(size_t)255);
+}
+
+int fa_decode_num_splits(int B, int H, int L, int d) {
+  (void)B;
+  (void)H;
+  (void)d;
+  return L > 0 ? 1 : 0;
+}
+
+fa_status fa_decode_splitkv(const void*, const void*, const void*, void*, float*, int, int, int, int, int, void*,
+                            float, fa_stream_t) {
+  return FA_ERR_UNSUPPORTED;
+}
+
+}  // extern "C"

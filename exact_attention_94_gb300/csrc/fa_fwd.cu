@@ -1,0 +1,424 @@
+// Forward kernel: exact attention with an online softmax on the fifth-generation
+// tensor cores (tcgen05) of sm_103a.
+//
+// Method ("13.14 FlashAttention: IO-aware exact attention", sections "Tile
+// decomposition" and "Online softmax"; FlashAttention-2 and its Blackwell
+// successor in "efficient-attention/flash-2-3"):
+//   for each block of 128 query rows Q_i, sweep the key/value blocks K_j, V_j:
+//     S = Q_i K_j^T                      (tensor cores, fp32 in Tensor Memory)
+//     m_new = max(m_ref, rowmax(S) * scale * log2 e)
+//     if m_new > m_ref + tau: O~ *= 2^(m_ref - m_new), l *= same, m_ref = m_new
+//     P = 2^(S * scale * log2 e - m_ref)  (bf16, written back over S in TMEM)
+//     l += rowsum(P);  O~ += P V_j         (tensor cores, A operand from TMEM)
+//   O = O~ / l,  lse = (m_ref + log2 l) * ln 2.
+// The conditional rescale ("And on Blackwell") keeps a stale reference
+// maximum until the true maximum has grown by more than 2^tau; l and O~ share
+// the reference, so the final division cancels it and the result is exact.
+// Part of the exponentials may be evaluated on the FMA pipe as
+// 2^floor(x) * p3(x - floor(x)) with a cubic fitted in fit_exp2_poly.py.
+//
+// CTA organisation (one CTA per pair of 128-row query tiles of one head):
+//   warp 0      TMA producer: Q tiles once, then K_j, V_j into a ring of slots
+//   warp 1      allocates TMEM; one lane issues every tcgen05.mma
+//   warps 4-7   softmax of query tile 0 (thread = row = TMEM lane)
+//   warps 8-11  softmax of query tile 1
+// The tensor pipe alternates between the two tiles (S0_j, PV1_{j-1}, S1_j,
+// PV0_j, ...) so one tile's softmax overlaps the other tile's products.
+// TMEM columns: S0 [0,128), S1 [128,256), O0 [256,256+d), O1 [256+d,256+2d).
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+#include <cmath>
+
+namespace fa {
+
+namespace {
+
+// Cubic for 2^f on [0, 1) with c0 = 1 (minimax relative error 8.6e-5),
+// produced by fit_exp2_poly.py.
+constexpr float kExp2C1 = 6.951168240e-01f;
+constexpr float kExp2C2 = 2.276448658e-01f;
+constexpr float kExp2C3 = 7.706713327e-02f;
+
+// 2^x on the FMA pipe: the integer part goes straight into the exponent field.
+__device__ __forceinline__ float ex2_poly(float x) {
+  x = fmaxf(x, -127.0f);
+  const float t = __fadd_rd(x, 12582912.0f);  // 1.5 * 2^23: floor(x) lands in the low mantissa bits
+  const float fl = t - 12582912.0f;           // floor(x), exact
+  const float f = x - fl;                      // [0, 1)
+  const float p = fmaf(fmaf(fmaf(kExp2C3, f, kExp2C2), f, kExp2C1), f, 1.0f);
+  return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
+}
+
+template <int D>
+struct FwdLayout {
+  static constexpr uint32_t kTile = 128u * D * 2u;   // one 128-row bf16 tile
+  static constexpr uint32_t kChunk = 128u * 128u;    // 128 rows x 64 bf16 (one 128-byte swizzle column)
+  static constexpr int kStages = D == 128 ? 4 : 8;    // K/V ring slots
+  static constexpr uint32_t kQOff = 0;
+  static constexpr uint32_t kKVOff = 2 * kTile;
+  static constexpr uint32_t kBarOff = kKVOff + kStages * kTile;
+  static constexpr uint32_t kBytes = kBarOff + 256 + 1024;  // barriers + alignment slack
+};
+
+constexpr int kThreads = 384;
+
+}  // namespace
+
+template <int D, bool CAUSAL, bool POLY>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using L = FwdLayout<D>;
+  constexpr int NS = L::kStages;
+  constexpr int CH = D / 64;
+  constexpr uint32_t TILE = L::kTile;
+  constexpr uint32_t CHUNK = L::kChunk;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sbase = smem_raw + (base - raw);
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+
+  // ---------------------------------------------------------------- work item
+  const int b = blockIdx.x / p.H;
+  const int h = blockIdx.x % p.H;
+  const int pair = p.num_pairs - 1 - (int)blockIdx.y;  // heaviest causal pairs first
+  int seq_start = 0, seq_len = p.seq_len, b_coord = b;
+  if (p.cu_seqlens != nullptr) {
+    seq_start = p.cu_seqlens[b];
+    seq_len = p.cu_seqlens[b + 1] - seq_start;
+    b_coord = 0;
+  }
+  const int q0 = pair * 256;
+  if (q0 >= seq_len) return;  // uniform for the CTA, before any shared state exists
+
+  const int n_kv_all = (seq_len + 127) / 128;
+  int nkv[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int r0 = q0 + 128 * t;
+    if (r0 >= seq_len) {
+      nkv[t] = 0;
+    } else if (CAUSAL) {
+      nkv[t] = min(n_kv_all, min(r0 + 127, seq_len - 1) / 128 + 1);
+    } else {
+      nkv[t] = n_kv_all;
+    }
+  }
+  const int nkv_max = max(nkv[0], nkv[1]);
+
+  // ---------------------------------------------------------------- barriers
+  enum { Q_FULL = 0, KV_FULL = 1, KV_EMPTY = 1 + NS, S_FULL = 1 + 2 * NS, P_FULL = S_FULL + 2, O_FINAL = P_FULL + 2,
+         DRAIN = O_FINAL + 2, NBARS = DRAIN + 1 };
+  const uint32_t bar0 = base + L::kBarOff;
+  auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + L::kBarOff + 8 * NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  if (threadIdx.x == 0) {
+    mbar_init(BAR(Q_FULL), 1);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(BAR(KV_FULL + i), 1);
+      mbar_init(BAR(KV_EMPTY + i), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(BAR(S_FULL + t), 1);
+      mbar_init(BAR(P_FULL + t), 128);
+      mbar_init(BAR(O_FINAL + t), 1);
+    }
+    mbar_init(BAR(DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtx w{abort_flag, p.timeout_ns, p.err};
+
+  const uint32_t q_s = base + L::kQOff;
+  const uint32_t kv_s = base + L::kKVOff;
+
+  if (warp == 0) {
+    // ============================================================ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(BAR(Q_FULL), 2 * TILE);
+      for (int t = 0; t < 2; ++t)
+        for (int c = 0; c < CH; ++c)
+          tma_load_4d(q_s + t * TILE + c * CHUNK, &tm_q, BAR(Q_FULL), c * 64, seq_start + q0 + 128 * t, h, b_coord);
+      bool ok = true;
+      for (int j = 0; j < nkv_max && ok; ++j) {
+        for (int which = 0; which < 2; ++which) {
+          const int u = 2 * j + which;
+          const int slot = u % NS;
+          if (u >= NS && !mbar_wait(BAR(KV_EMPTY + slot), ((u / NS) - 1) & 1, w, 1)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(BAR(KV_FULL + slot), TILE);
+          const CUtensorMap* m = which ? &tm_v : &tm_k;
+          for (int c = 0; c < CH; ++c)
+            tma_load_4d(kv_s + slot * TILE + c * CHUNK, m, BAR(KV_FULL + slot), c * 64, seq_start + 128 * j, h,
+                        b_coord);
+        }
+      }
+      if (!ok) {  // let copies already in flight land before the CTA's shared memory goes away
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 200000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ============================================================ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t IDESC_O = idesc_bf16(128, D, false, true);
+      const uint32_t tS0 = tmem, tS1 = tmem + 128;
+      const uint32_t tO0 = tmem + 256, tO1 = tmem + 256 + D;
+      bool ok = true;
+
+      // S_t = Q_t K^T: both operands K-major, 128-byte swizzle; K=16 per instruction
+      auto issue_S = [&](int t, int slot) {
+        const uint32_t qa = q_s + t * TILE, ka = kv_s + slot * TILE;
+        const uint32_t dst = t ? tS1 : tS0;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * CHUNK + (kk % 4) * 32;
+          mma_ss(dst, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024), IDESC_S, kk > 0);
+        }
+      };
+      // O_t += P_t V: P from TMEM (bf16 pairs over S_t's columns), V MN-major from shared memory
+      auto issue_PV = [&](int t, int slot, bool acc) {
+        const uint32_t va = kv_s + slot * TILE;
+        const uint32_t dst = t ? tO1 : tO0;
+        const uint32_t pa = t ? tS1 : tS0;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(dst, pa + kk * 8, smem_desc_sw128(va + kk * 2048, CHUNK, 1024), IDESC_O, (acc || kk > 0) ? 1u : 0u);
+      };
+
+      ok = mbar_wait(BAR(Q_FULL), 0, w, 2);
+      tc_fence_after();
+      for (int j = 0; j < nkv_max && ok; ++j) {
+        const int uk = 2 * j, sk = uk % NS;
+        if (!(ok = mbar_wait(BAR(KV_FULL + sk), (uk / NS) & 1, w, 3))) break;
+        tc_fence_after();
+        if (j < nkv[0]) {
+          issue_S(0, sk);
+          mma_commit(BAR(S_FULL + 0));
+        }
+        if (j >= 1) {
+          const int sv = (2 * (j - 1) + 1) % NS;
+          if (j - 1 < nkv[1]) {
+            if (!(ok = mbar_wait(BAR(P_FULL + 1), (j - 1) & 1, w, 4))) break;
+            tc_fence_after();
+            issue_PV(1, sv, j - 1 > 0);
+            if (j - 1 == nkv[1] - 1) mma_commit(BAR(O_FINAL + 1));
+          }
+          mma_commit(BAR(KV_EMPTY + sv));
+        }
+        if (j < nkv[1]) {
+          issue_S(1, sk);
+          mma_commit(BAR(S_FULL + 1));
+        }
+        mma_commit(BAR(KV_EMPTY + sk));
+        const int uv = 2 * j + 1, sv = uv % NS;
+        if (!(ok = mbar_wait(BAR(KV_FULL + sv), (uv / NS) & 1, w, 5))) break;
+        tc_fence_after();
+        if (j < nkv[0]) {
+          if (!(ok = mbar_wait(BAR(P_FULL + 0), j & 1, w, 6))) break;
+          tc_fence_after();
+          issue_PV(0, sv, j > 0);
+          if (j == nkv[0] - 1) mma_commit(BAR(O_FINAL + 0));
+        }
+      }
+      if (ok && nkv_max >= 1) {
+        const int j = nkv_max;
+        const int sv = (2 * (j - 1) + 1) % NS;
+        if (j - 1 < nkv[1]) {
+          if ((ok = mbar_wait(BAR(P_FULL + 1), (j - 1) & 1, w, 4))) {
+            tc_fence_after();
+            issue_PV(1, sv, j - 1 > 0);
+            mma_commit(BAR(O_FINAL + 1));
+          }
+        }
+        if (ok) mma_commit(BAR(KV_EMPTY + sv));
+      }
+      // Drain: every product and every earlier commit's arrival has landed
+      // before TMEM is released and the CTA's shared memory goes away.
+      mma_commit(BAR(DRAIN));
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(BAR(DRAIN), 0) && globaltimer_ns() - t0 < p.timeout_ns) {
+      }
+    }
+  } else if (warp >= 4) {
+    // ============================================================ softmax
+    const int t = (warp - 4) >> 2;
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const int row = q0 + 128 * t + r;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + (t ? 128u : 0u);
+    const uint32_t tO = tmem + lane_off + 256u + (t ? (uint32_t)D : 0u);
+    const float sl2 = p.scale_log2;
+    const float tau = p.tau;
+    float m_ref = -INFINITY;
+    float l = 0.f;
+    bool ok = true;
+
+    for (int j = 0; j < nkv[t]; ++j) {
+      ok = mbar_wait(BAR(S_FULL + t), j & 1, w, 7);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sr[c]);
+      tmem_ld_wait();
+      float x[128];
+#pragma unroll
+      for (int i = 0; i < 128; ++i) x[i] = __uint_as_float(sr[i / 32][i % 32]);
+
+      const int kv0 = 128 * j;
+      const int lim = CAUSAL ? min(row + 1, seq_len) : seq_len;  // visible keys are < lim
+      if (kv0 + 128 > lim) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (kv0 + i >= lim) x[i] = -INFINITY;
+      }
+      float mx = x[0];
+#pragma unroll
+      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, x[i]);
+      const float m_new = mx * sl2;
+      float alpha = 1.f;
+      const bool resc = m_new > m_ref + tau;
+      if (resc) {
+        alpha = ex2_sfu(m_ref - m_new);
+        m_ref = m_new;
+      }
+      const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
+
+      uint32_t pk[2][32];
+      float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        float p0, p1;
+        if (POLY && (i & 3) == 3) {
+          p0 = ex2_poly(fmaf(x[2 * i], sl2, -mb));
+          p1 = ex2_poly(fmaf(x[2 * i + 1], sl2, -mb));
+        } else {
+          p0 = ex2_sfu(fmaf(x[2 * i], sl2, -mb));
+          p1 = ex2_sfu(fmaf(x[2 * i + 1], sl2, -mb));
+        }
+        sum0 += p0;
+        sum1 += p1;
+        pk[i / 32][i % 32] = pack_bf16x2(p0, p1);
+      }
+      l = l * alpha + (sum0 + sum1);
+
+      if (j > 0 && __any_sync(0xffffffffu, resc)) {
+        // rows whose reference moved: O~ *= alpha (alpha = 1 for the others)
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(tO + 32 * c, ov);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+          tmem_st32(tO + 32 * c, ov);
+        }
+      }
+      tmem_st32(tS, pk[0]);
+      tmem_st32(tS + 32, pk[1]);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(BAR(P_FULL + t));
+    }
+
+    // ------------------------------------------------------------ epilogue
+    if (ok && nkv[t] > 0) {
+      ok = mbar_wait(BAR(O_FINAL + t), 0, w, 8);
+      if (__all_sync(0xffffffffu, ok)) {
+        tc_fence_after();
+        const bool row_ok = row < seq_len;
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) +
+                              (((size_t)b_coord * p.n_rows + seq_start + row) * p.H + h) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(tO + 32 * c, ov);
+          tmem_ld_wait();
+          uint32_t pkd[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pkd[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
+          if (row_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
+          }
+        }
+        if (row_ok) {
+          const float lse = l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+          p.lse[((size_t)b_coord * p.H + h) * p.n_rows + seq_start + row] = lse;
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool CAUSAL, bool POLY>
+static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const FwdParams& p, int grid_x, cudaStream_t stream) {
+  auto kern = fa_fwd_kernel<D, CAUSAL, POLY>;
+  constexpr uint32_t smem = FwdLayout<D>::kBytes;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  dim3 grid(grid_x, p.num_pairs);
+  kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
+                       int D, bool causal, bool poly, int grid_x, cudaStream_t stream) {
+#define FA_FWD_CASE(DD, CC, PP) \
+  if (D == DD && causal == CC && poly == PP) return launch_fwd_t<DD, CC, PP>(tq, tk, tv, p, grid_x, stream);
+  FA_FWD_CASE(64, false, false)
+  FA_FWD_CASE(64, false, true)
+  FA_FWD_CASE(64, true, false)
+  FA_FWD_CASE(64, true, true)
+  FA_FWD_CASE(128, false, false)
+  FA_FWD_CASE(128, false, true)
+  FA_FWD_CASE(128, true, false)
+  FA_FWD_CASE(128, true, true)
+#undef FA_FWD_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

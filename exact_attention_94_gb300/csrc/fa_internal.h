@@ -1,0 +1,65 @@
+// Host-side launch interfaces shared between the C-ABI layer and the kernel
+// translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace fa {
+
+struct FwdParams {
+  void* o;                   // bf16 output
+  float* lse;                // fp32 log-sum-exp
+  const int* cu_seqlens;     // packed batch offsets (device) or nullptr for a dense batch
+  int H;
+  int n_rows;                // rows along the sequence axis of the tensors (N, or total tokens)
+  int seq_len;               // dense: N
+  int num_pairs;             // grid.y: pairs of 128-row query tiles per (sequence, head)
+  float scale_log2;          // scale * log2(e)
+  float tau;                 // lazy-rescale threshold, log2 units
+  unsigned* err;             // device error word
+  unsigned long long timeout_ns;
+};
+
+struct BwdParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const void* dout;
+  const float* lse;
+  float* dsum;               // D_i, [B, H, N] / [H, total]
+  float* dq_acc;             // fp32 accumulator, same layout as q
+  void* dq;
+  void* dk;
+  void* dv;
+  const int* cu_seqlens;
+  int B;                     // dense batch, or number of sequences
+  int H;
+  int n_rows;
+  int seq_len;
+  int num_kblocks;           // grid.y of the main kernel
+  float scale;
+  float scale_log2;
+  unsigned* err;
+  unsigned long long timeout_ns;
+};
+
+// Encodes a 4-D bf16 tensor map over [B][n_rows][H][D] with a 128-row x 64-column
+// box and 128-byte swizzle.  Returns false when the driver refuses it.
+bool make_tmap_bhnd(CUtensorMap* m, const void* ptr, int D, int n_rows, int H, int B);
+
+cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
+                       int D, bool causal, bool poly, int grid_x, cudaStream_t stream);
+
+cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const BwdParams& p, int D, bool causal, int grid_x,
+                       cudaStream_t stream);
+
+cudaError_t launch_decode(const void* q, const void* k, const void* v, void* o, float* lse, float* part_o,
+                          float* part_lse, int B, int H, int L, int D, int num_splits, float scale_log2,
+                          cudaStream_t stream);
+
+}  // namespace fa

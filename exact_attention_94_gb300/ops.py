@@ -1,0 +1,164 @@
+"""PyTorch-facing wrappers of the C ABI (argument marshalling only).
+
+Every function checks dtypes, devices, shapes and contiguity, allocates the
+outputs with torch (PyTorch is the device-memory and stream provider here),
+and calls the matching ``fa_*`` entry point on the current CUDA stream.  All
+arithmetic happens in the library's CUDA kernels.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from typing import Optional, Tuple
+
+import torch
+
+from . import _lib
+
+_lib_handle = None
+
+
+def lib():
+    global _lib_handle
+    if _lib_handle is None:
+        _lib_handle = _lib.load()
+    return _lib_handle
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check_bf16(name, t, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def set_option(opt: int, value: float) -> None:
+    _lib.check(lib().fa_set_option(opt, float(value)), "fa_set_option")
+
+
+def device_error() -> int:
+    """Synchronises and returns the recorded device error code (0 = none)."""
+    code = ctypes.c_uint(0)
+    lib().fa_device_error(ctypes.byref(code))
+    return int(code.value)
+
+
+def fwd(q, k, v, causal: bool = False, scale: Optional[float] = None, out=None, lse=None,
+        stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Dense forward.  q, k, v [B, N, H, d] bf16 -> (o [B, N, H, d], lse [B, H, N] fp32)."""
+    _check_bf16("q", q)
+    B, N, H, d = q.shape
+    _check_bf16("k", k, q.shape)
+    _check_bf16("v", v, q.shape)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check_bf16("out", o, q.shape)
+    st = lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, H, N, d, int(bool(causal)), scale,
+                      _stream(stream))
+    _lib.check(st, "fa_fwd")
+    return o, l
+
+
+def bwd(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float] = None, workspace=None,
+        stream=None):
+    """Dense backward -> (dq, dk, dv), each [B, N, H, d] bf16."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _check_bf16(name, t, q.shape)
+    B, N, H, d = q.shape
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous fp32 [B, H, N]")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    nbytes = lib().fa_bwd_workspace_bytes(B, H, N, d)
+    ws = workspace if workspace is not None else torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    if ws.numel() * ws.element_size() < nbytes:
+        raise ValueError("workspace too small")
+    st = lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                      _ptr(ws), B, H, N, d, int(bool(causal)), scale, _stream(stream))
+    _lib.check(st, "fa_bwd")
+    return dq, dk, dv
+
+
+def _check_cu(cu_seqlens, q):
+    if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or not cu_seqlens.is_contiguous():
+        raise ValueError("cu_seqlens must be a contiguous int32 CUDA tensor")
+    if cu_seqlens.device != q.device:
+        raise ValueError("cu_seqlens must be on the device of q")
+
+
+def fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False, scale: Optional[float] = None,
+               stream=None):
+    """Packed forward.  q, k, v [total, H, d]; cu_seqlens int32 [S+1] on the device.
+    Returns (o [total, H, d], lse [H, total])."""
+    _check_bf16("q", q)
+    total, H, d = q.shape
+    _check_bf16("k", k, q.shape)
+    _check_bf16("v", v, q.shape)
+    _check_cu(cu_seqlens, q)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q)
+    l = torch.empty((H, total), dtype=torch.float32, device=q.device)
+    st = lib().fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), _ptr(cu_seqlens), cu_seqlens.numel() - 1,
+                             int(max_seqlen), total, H, d, int(bool(causal)), scale, _stream(stream))
+    _lib.check(st, "fa_fwd_varlen")
+    return o, l
+
+
+def bwd_varlen(q, k, v, o, lse, dout, cu_seqlens, max_seqlen: int, causal: bool = False,
+               scale: Optional[float] = None, stream=None):
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _check_bf16(name, t, q.shape)
+    total, H, d = q.shape
+    _check_cu(cu_seqlens, q)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (H, total) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous fp32 [H, total]")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    nbytes = lib().fa_bwd_varlen_workspace_bytes(total, H, d)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    st = lib().fa_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                             _ptr(dv), _ptr(ws), _ptr(cu_seqlens), cu_seqlens.numel() - 1, int(max_seqlen), total,
+                             H, d, int(bool(causal)), scale, _stream(stream))
+    _lib.check(st, "fa_bwd_varlen")
+    return dq, dk, dv
+
+
+def decode(q, k_cache, v_cache, num_splits: int = 0, scale: Optional[float] = None, stream=None,
+           workspace=None):
+    """Single-token decode.  q [B, 1, H, d]; caches [B, L, H, d].
+    Returns (o [B, 1, H, d], lse [B, H])."""
+    _check_bf16("q", q)
+    B, one, H, d = q.shape
+    if one != 1:
+        raise ValueError("q must be [B, 1, H, d]")
+    _check_bf16("k_cache", k_cache)
+    L = k_cache.shape[1]
+    if tuple(k_cache.shape) != (B, L, H, d):
+        raise ValueError("k_cache must be [B, L, H, d]")
+    _check_bf16("v_cache", v_cache, k_cache.shape)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    splits = num_splits if num_splits > 0 else lib().fa_decode_num_splits(B, H, L, d)
+    nbytes = lib().fa_decode_workspace_bytes(B, H, d, max(splits, 1))
+    ws = workspace if workspace is not None else torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    o = torch.empty_like(q)
+    l = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    st = lib().fa_decode_splitkv(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(l), B, H, L, d, splits,
+                                 _ptr(ws), scale, _stream(stream))
+    _lib.check(st, "fa_decode_splitkv")
+    return o, l

@@ -1,0 +1,173 @@
+/*
+ * fa.h -- C ABI of the exact-attention library for GB300 (sm_103a), libfa.so.
+ *
+ * Exact softmax attention O = softmax(scale * Q K^T [+ causal mask]) V computed
+ * tile by tile with an online softmax, so the n x n score and probability
+ * matrices never reach device memory.
+ *
+ * Sources for what each call computes:
+ *  - "13.14 FlashAttention: IO-aware exact attention" (textbookofai.com),
+ *    sections "Tile decomposition" and "Online softmax": the tiled one-pass
+ *    algorithm and its exactness; "Backpropagation uses the same trick": the
+ *    backward recomputes tiles instead of storing P.
+ *  - "efficient-attention/flash-2-3" (zerotofrontier.app), sections
+ *    "Fewer non-matmul FLOPs" (unnormalised output, one division at the end,
+ *    lse = m + log l kept for the backward, e^(s - lse) recomputed),
+ *    "Parallelism over the sequence" (grid over query blocks x batch*heads;
+ *    backward over key blocks with dQ added atomically), "Decoding needs a
+ *    different split" (split-KV partials and the log-sum-exp merge),
+ *    "Variable-length batches without padding" (packed rows + cu_seqlens),
+ *    "Using it, the real way" (flash-attn's (batch, T, heads, d_k) layout).
+ *
+ * Conventions shared by every call
+ *  - Element type: bf16 for Q, K, V, O, dO, dQ, dK, dV; fp32 for lse.
+ *  - Dense layout [B, N, H, d] contiguous (d fastest); packed layout
+ *    [total, H, d]; lse [B, H, N] dense, [H, total] packed, [B, H] decode.
+ *  - lse is the natural log of sum_j exp(scale * q . k_j) (scale included).
+ *  - causal: key j is visible to query i iff j <= i (queries and keys have
+ *    the same length in every causal call, where the top-left and
+ *    bottom-right alignments coincide).
+ *  - Supported head dims: d in {64, 128}.
+ *  - Ownership: the caller allocates and owns every buffer (device memory);
+ *    the library allocates nothing.  Calls that need scratch memory take a
+ *    caller-provided workspace sized by the matching *_workspace_bytes().
+ *  - Asynchrony: every call only enqueues work on `stream` and returns.
+ *  - Errors: arguments are validated on the host before any launch; on an
+ *    error nothing is launched and no output is touched.  Device pointers
+ *    must be 16-byte aligned (FA_ERR_MISALIGNED otherwise).  A launch failure
+ *    gives FA_ERR_LAUNCH.  Every wait inside the kernels is bounded; a wait
+ *    that runs out records a code that fa_device_error() returns
+ *    (FA_ERR_TIMEOUT) instead of hanging the GPU.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* fa_stream_t; /* same handle as cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* a size, count or scale out of range, a null pointer */
+  FA_ERR_UNSUPPORTED = 2, /* head dim not in {64, 128}, device not sm_103 */
+  FA_ERR_MISALIGNED = 3,  /* a device pointer not 16-byte aligned */
+  FA_ERR_LAUNCH = 4,      /* the CUDA runtime refused a launch */
+  FA_ERR_TIMEOUT = 5      /* a bounded wait inside a kernel ran out */
+} fa_status;
+
+/* Human-readable name of a status code (static storage). */
+const char* fa_status_string(fa_status s);
+
+/*
+ * Forward pass, dense batch.  ("Tile decomposition", "Online softmax";
+ * FlashAttention-2 "Fewer non-matmul FLOPs".)
+ *   q, k, v : [B, N, H, d] bf16, device, read only
+ *   o       : [B, N, H, d] bf16, device, written
+ *   lse     : [B, H, N] fp32, device, written (natural log, scale included)
+ *   causal  : 0 or 1
+ *   scale   : multiplies Q K^T before the softmax (> 0, finite)
+ * B, H >= 1 and N >= 0 (N == 0 is a no-op).
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                 int causal, float scale, fa_stream_t stream);
+
+/*
+ * Scratch bytes fa_bwd needs: an fp32 dQ accumulator [B, N, H, d] and the
+ * row sums D_i = sum_k dO_ik O_ik [B, H, N] fp32.
+ */
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * Backward pass, dense batch.  (Backpropagation "recomputes the relevant
+ * tiles"; FlashAttention-2: weights recomputed as e^(s - lse), parallel over
+ * key blocks, dQ added atomically.)
+ *   q, k, v, o : [B, N, H, d] bf16 (o from fa_fwd)
+ *   lse        : [B, H, N] fp32 from fa_fwd
+ *   dout       : [B, N, H, d] bf16, gradient of the loss with respect to O
+ *   dq, dk, dv : [B, N, H, d] bf16, written
+ *   workspace  : fa_bwd_workspace_bytes(B, H, N, d) bytes, device, 16-byte
+ *                aligned; contents on entry do not matter
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                 void* dq, void* dk, void* dv, void* workspace, int B, int H, int N, int d, int causal, float scale,
+                 fa_stream_t stream);
+
+/*
+ * Forward pass, packed variable-length batch ("Variable-length batches
+ * without padding").  Sequence b owns rows cu_seqlens[b] .. cu_seqlens[b+1]-1
+ * and attends only within them; tiles between sequences are never visited.
+ *   q, k, v    : [total_tokens, H, d] bf16
+ *   o          : [total_tokens, H, d] bf16, written
+ *   lse        : [H, total_tokens] fp32, written
+ *   cu_seqlens : int32 [num_seqs + 1], DEVICE memory, non-decreasing,
+ *                cu_seqlens[0] = 0, cu_seqlens[num_seqs] = total_tokens
+ *   max_seqlen : an upper bound of every sequence length (sizes the grid;
+ *                rows of a longer sequence beyond it are not computed)
+ */
+fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
+                        int num_seqs, int max_seqlen, int total_tokens, int H, int d, int causal, float scale,
+                        fa_stream_t stream);
+
+/* Scratch bytes fa_bwd_varlen needs (same two buffers over total_tokens rows). */
+size_t fa_bwd_varlen_workspace_bytes(int total_tokens, int H, int d);
+
+/* Backward pass of fa_fwd_varlen; tensors as in fa_bwd in the packed layout. */
+fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                        const void* dout, void* dq, void* dk, void* dv, void* workspace, const int* cu_seqlens,
+                        int num_seqs, int max_seqlen, int total_tokens, int H, int d, int causal, float scale,
+                        fa_stream_t stream);
+
+/*
+ * Scratch bytes fa_decode_splitkv needs for num_splits partial results:
+ * fp32 O_c [B, H, num_splits, d] and lse_c [B, H, num_splits].
+ */
+size_t fa_decode_workspace_bytes(int B, int H, int d, int num_splits);
+
+/* Number of splits fa_decode_splitkv uses when it is given num_splits = 0. */
+int fa_decode_num_splits(int B, int H, int L, int d);
+
+/*
+ * Single-token decode with a split KV cache ("Decoding needs a different
+ * split"): each chunk of the cache yields a partial (O_c, lse_c), and a
+ * second kernel merges them, lse = log sum_c e^lse_c and
+ * O = sum_c e^(lse_c - lse) O_c.
+ *   q                : [B, 1, H, d] bf16
+ *   k_cache, v_cache : [B, L, H, d] bf16
+ *   o                : [B, 1, H, d] bf16, written
+ *   lse              : [B, H] fp32, written
+ *   num_splits       : 0 = choose (fa_decode_num_splits); else 1..L
+ *   workspace        : fa_decode_workspace_bytes(B, H, d, splits) bytes
+ */
+fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse, int B,
+                            int H, int L, int d, int num_splits, void* workspace, float scale, fa_stream_t stream);
+
+/*
+ * Synchronises the device, then returns FA_OK if no kernel of this library
+ * recorded an error since the last call, FA_ERR_TIMEOUT if a bounded wait ran
+ * out (the recorded code, which names the wait site, goes to *code when code
+ * is not NULL).  Clears the recorded code.
+ */
+fa_status fa_device_error(unsigned int* code);
+
+/*
+ * Developer knobs (process-wide; they change speed, not results beyond
+ * rounding):
+ *   FA_OPT_RESCALE_TAU   : lazy-rescale threshold in log2 units (default 8;
+ *                          0 rescales whenever the running maximum grows)
+ *   FA_OPT_POLY_EXP      : 1 = evaluate a share of the exponentials with the
+ *                          cubic on the FMA pipe, 0 = all on the SFU
+ *   FA_OPT_WAIT_TIMEOUT_MS : limit of every bounded wait (default 2000)
+ */
+typedef enum { FA_OPT_RESCALE_TAU = 1, FA_OPT_POLY_EXP = 2, FA_OPT_WAIT_TIMEOUT_MS = 3 } fa_option;
+fa_status fa_set_option(fa_option opt, double value);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */
