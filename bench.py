@@ -1,0 +1,479 @@
+#!/usr/bin/env python
+"""Benchmark of the exact-attention library on one GB300 (or N replicas).
+
+Metric: attention TFLOP/s for forward and forward+backward, bf16, on the long
+workload (B=2, H=16, N=8192, d=128, causal, K x 3 in heads 0-7).  FLOPs are
+4*B*H*N^2*d for the forward, halved for causal, and 2.5x that for the
+backward.  A step is one forward (fa_fwd) plus one backward (fa_bwd) over the
+same inputs, which are resident in device memory when the timed region starts.
+Q, K, V and dO are 67 MB each (268 MB together), larger than the 129 MB L2,
+so no L2 flush is needed between steps.
+
+Launch:  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+For N > 1 the driver starts one process per GPU with torchrun; every rank
+runs the same workload on its own GPU (independent replicas: the units of this
+path, (batch, head) pairs, need no exchange), and rank 0 prints one JSON line
+with the total work of all ranks divided by the slowest rank's time.
+
+``--impl reference`` times the float64 CPU oracle (the correctness baseline)
+on the machine's host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+N_CORES = len(os.sched_getaffinity(0))
+# The oracle's BLAS must use exactly the host cores we report.
+os.environ.setdefault("OPENBLAS_NUM_THREADS", str(N_CORES))
+os.environ.setdefault("OMP_NUM_THREADS", str(N_CORES))
+
+METRIC = "attention TFLOP/s fwd & fwd+bwd (bf16, d=128, N=8k causal), % of tensor peak"
+LONG = dict(B=2, H=16, N=8192, d=128, causal=True, k_boost=3.0)
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads' sub-measurements")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = None
+        self.gpu = gpu_index
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]) if parts[3] not in ("[N/A]", "N/A") else 0.0,
+                             parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [r for r in rows if r[2] > 0.5 * max(x[2] for x in rows)] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(loaded)}
+
+
+# ---------------------------------------------------------------- helpers
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def source_sha(*names):
+    h = hashlib.sha256()
+    for n in names:
+        h.update(open(os.path.join(ROOT, "exact_attention_94_gb300", "csrc", n), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(summary_name, sources):
+    """DRAM bytes per launch from a committed ncu summary, or None when the
+    kernel's sources changed after the counters were taken."""
+    path = os.path.join(ROOT, "profiles", summary_name)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_sha = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_b or m_sha.group(1) != source_sha(*sources):
+        return None
+    return float(m_b.group(1))
+
+
+class Timer:
+    """CUDA events on the current (launching) stream."""
+
+    def __init__(self, torch):
+        self.t = torch
+        self.ev = []
+
+    def mark(self):
+        e = self.t.cuda.Event(enable_timing=True)
+        e.record()
+        self.ev.append(e)
+        return e
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import synth
+    from exact_attention_94_gb300 import _lib, accounting as acc, ops
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    ops.lib()
+    peaks = load_peaks()
+    w = LONG
+    B, H, N, d, causal = w["B"], w["H"], w["N"], w["d"], w["causal"]
+    F = acc.fwd_flops(B, H, N, d, causal)
+    x = synth.make_dense(B, H, N, d, seed=0, k_boost=w["k_boost"], device="cuda")
+    q, k, v, do = x["q"], x["k"], x["v"], x["do"]
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    ws = torch.empty(ops.lib().fa_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device="cuda")
+    have_bwd = True
+    ops.fwd(q, k, v, causal=causal, out=o, lse=lse)
+    try:
+        ops.bwd(q, k, v, o, lse, do, causal=causal, workspace=ws)
+    except _lib.FaError as e:
+        if e.status != _lib.FA_ERR_UNSUPPORTED:
+            raise
+        have_bwd = False
+    torch.cuda.synchronize()
+
+    def step(tm=None):
+        if tm is not None:
+            tm.mark()
+        ops.fwd(q, k, v, causal=causal, out=o, lse=lse)
+        if tm is not None:
+            tm.mark()
+        if have_bwd:
+            ops.bwd(q, k, v, o, lse, do, causal=causal, workspace=ws)
+            if tm is not None:
+                tm.mark()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    tm = Timer(torch)
+    with ClockSampler(local) as clocks:
+        torch.cuda.synchronize()
+        start = tm.mark()
+        inner = Timer(torch)
+        for _ in range(args.steps):
+            step(inner)
+        end = tm.mark()
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    total_ms = start.elapsed_time(end)
+    per = 3 if have_bwd else 2
+    fwd_ms = [inner.ev[i * per].elapsed_time(inner.ev[i * per + 1]) for i in range(args.steps)]
+    bwd_ms = ([inner.ev[i * per + 1].elapsed_time(inner.ev[i * per + 2]) for i in range(args.steps)]
+              if have_bwd else [0.0])
+    if world > 1:
+        t = torch.tensor([total_ms, statistics.mean(fwd_ms), statistics.mean(bwd_ms)], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, fwd_mean, bwd_mean = t.tolist()
+    else:
+        fwd_mean, bwd_mean = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
+    assert ops.device_error() == 0, "a bounded wait ran out inside a kernel"
+    ms_step = total_ms / args.steps
+    step_flops = F * (2.5 if have_bwd else 1.0)     # literal reading: fwd+bwd = 2.5x the forward
+    value = world * step_flops / (ms_step * 1e-3) / 1e12
+    fwd_tf = F / (fwd_mean * 1e-3) / 1e12
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "long: B=2 H=16 N=8192 d=128 causal, K x3 in heads 0-7",
+                   "step": "fa_fwd + fa_bwd" if have_bwd else "fa_fwd only (fa_bwd not built)",
+                   "flops_convention": "fwd 4BHN^2d/2; fwd+bwd 2.5x fwd",
+                   "l2": "inputs 268 MB > 129 MB L2, no flush", "parallelism": f"replicas x{world}"},
+        "fwd_tflops": round(fwd_tf, 2),
+        "fwd_frac_of_peak": round(fwd_tf / peaks["bf16_tflops"], 4),
+        "fwdbwd_frac_of_peak": round(value / world / peaks["bf16_tflops"], 4),
+    }
+    if have_bwd:
+        res["fwdbwd_tflops_3p5x"] = round(world * 3.5 * F / (ms_step * 1e-3) / 1e12, 2)
+        res["bwd_tflops"] = round(2.5 * F / (bwd_mean * 1e-3) / 1e12, 2)
+    # roofline of the dominant kernel (largest share of the step)
+    if have_bwd and bwd_mean > fwd_mean:
+        ach = 2.5 * F / (bwd_mean * 1e-3) / 1e12
+        traffic = profiled_traffic("fa_bwd_long.md", ["fa_bwd.cu", "ptx.cuh"])
+        kname = "fa_bwd (main + pre/post kernels, timed together)"
+    else:
+        ach = fwd_tf
+        traffic = profiled_traffic("fa_fwd_long.md", ["fa_fwd.cu", "ptx.cuh"])
+        kname = "fa_fwd_kernel"
+    res["roofline"] = {"kernel": kname, "bound": "tensor", "achieved": round(ach, 2), "peak": peaks["bf16_tflops"],
+                       "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4), "traffic": traffic,
+                       "peak_source": f"{peaks['source']} bf16 burst"}
+    res["clocks"] = clocks.summary()
+    res["gpu_launches"] = args.steps * (1 + (3 if have_bwd else 0))
+    return res, (x, o, lse, ws, have_bwd, F)
+
+
+def run_e2e(args, ctx):
+    """Same metric through the public API with host buffers: every step copies
+    q, k, v, dO from pinned host memory and reads o, lse, dq, dk, dv back."""
+    import torch
+
+    from exact_attention_94_gb300 import accounting as acc, ops
+
+    x, o, lse, ws, have_bwd, F = ctx
+    w = LONG
+    host = {n: x[n].cpu().pin_memory() for n in ("q", "k", "v", "do")}
+    dev = {n: torch.empty_like(x[n]) for n in host}
+    outs_dev = {}
+    outs_host = {}
+
+    def step():
+        for n in host:
+            dev[n].copy_(host[n], non_blocking=True)
+        od, ld = ops.fwd(dev["q"], dev["k"], dev["v"], causal=w["causal"])
+        outs_dev["o"], outs_dev["lse"] = od, ld
+        if have_bwd:
+            dq, dk, dv = ops.bwd(dev["q"], dev["k"], dev["v"], od, ld, dev["do"], causal=w["causal"], workspace=ws)
+            outs_dev.update(dq=dq, dk=dk, dv=dv)
+        for n, t in outs_dev.items():
+            if n not in outs_host:
+                outs_host[n] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            outs_host[n].copy_(t, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    steps = max(3, args.steps // 2)
+    s.record()
+    for _ in range(steps):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    flops = F * (2.5 if have_bwd else 1.0)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs_host.values())
+    return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def time_calls(torch, fn, warm=2, iters=5):
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(iters):
+        fn()
+    e.record()
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / iters
+
+
+def run_extra(peaks):
+    """Short measurements of the other workloads (the headline is the long one)."""
+    import torch
+
+    import synth
+    from exact_attention_94_gb300 import _lib, accounting as acc, ops
+
+    out = {}
+    # mid: B16 H16 N2048 d64 non-causal
+    w = synth.WORKLOADS["mid"]
+    x = synth.make_dense(w.B, w.H, w.N, w.d, seed=0, device="cuda")
+    F = acc.fwd_flops(w.B, w.H, w.N, w.d, False)
+    o, lse = ops.fwd(x["q"], x["k"], x["v"])
+    t_f = time_calls(torch, lambda: ops.fwd(x["q"], x["k"], x["v"], out=o, lse=lse))
+    r = {"fwd_ms": round(t_f, 4), "fwd_tflops": round(F / t_f / 1e9, 1)}
+    try:
+        t_b = time_calls(torch, lambda: ops.bwd(x["q"], x["k"], x["v"], o, lse, x["do"]))
+        r.update(bwd_ms=round(t_b, 4), fwdbwd_tflops=round(2.5 * F / (t_f + t_b) / 1e9, 1))
+    except _lib.FaError:
+        pass
+    out["mid"] = r
+    del x, o, lse
+    # varlen: 32 seeded lengths in [128, 4096], H32 d128 causal
+    w = synth.WORKLOADS["varlen"]
+    lengths = synth.varlen_lengths(w.B, w.len_lo, w.len_hi, w.seed)
+    x = synth.make_varlen(lengths, w.H, w.d, seed=0, device="cuda")
+    cu = x["cu_seqlens"].cuda()
+    F = acc.varlen_fwd_flops(lengths.tolist(), w.H, w.d, True)
+    mx = int(lengths.max())
+    o, lse = ops.fwd_varlen(x["q"], x["k"], x["v"], cu, mx, causal=True)
+    t_f = time_calls(torch, lambda: ops.fwd_varlen(x["q"], x["k"], x["v"], cu, mx, causal=True))
+    r = {"tokens": int(lengths.sum()), "fwd_ms": round(t_f, 4), "fwd_tflops": round(F / t_f / 1e9, 1)}
+    try:
+        t_b = time_calls(torch, lambda: ops.bwd_varlen(x["q"], x["k"], x["v"], o, lse, x["do"], cu, mx, causal=True))
+        r.update(bwd_ms=round(t_b, 4), fwdbwd_tflops=round(2.5 * F / (t_f + t_b) / 1e9, 1))
+    except _lib.FaError:
+        pass
+    out["varlen"] = r
+    del x, o, lse
+    # decode: B64 L32768 H32 d128 (34.4 GB of K/V, far larger than L2)
+    w = synth.WORKLOADS["decode"]
+    try:
+        x = synth.make_decode(w.B, w.H, w.N, w.d, seed=0, device="cuda")
+        ops.decode(x["q"], x["k"], x["v"])
+        t = time_calls(torch, lambda: ops.decode(x["q"], x["k"], x["v"]), warm=2, iters=5)
+        byts = acc.decode_bytes(w.B, w.H, w.N, w.d)
+        out["decode"] = {"ms": round(t, 4), "GB/s": round(byts / t / 1e6, 1),
+                         "frac_of_hbm": round(byts / t / 1e6 / peaks["hbm_gbs"], 4)}
+        del x
+    except _lib.FaError:
+        pass
+    torch.cuda.empty_cache()
+    return out
+
+
+def cpu_sample(heads):
+    """Float64 oracle forward+backward on a few (b, h) heads of the long
+    workload; returns (TFLOP/s under the metric's convention, seconds)."""
+    import numpy as np
+
+    import oracle
+    import synth
+    from exact_attention_94_gb300 import accounting as acc
+
+    w = LONG
+    if "x" not in _CPU_INPUTS:  # generated once, outside every timed region
+        _CPU_INPUTS["x"] = synth.make_dense(w["B"], w["H"], w["N"], w["d"], seed=0, k_boost=w["k_boost"])
+    x = _CPU_INPUTS["x"]
+    scale = 1.0 / math.sqrt(w["d"])
+    per_head = [tuple(synth.to_f64(x[n][b, :, h]) for n in ("q", "k", "v", "do")) for b, h in heads]
+    t0 = time.perf_counter()
+    for qh, kh, vh, dh in per_head:
+        oracle.head_forward(qh, kh, vh, scale, True)
+        oracle.head_backward(qh, kh, vh, dh, scale, True)
+    sec = time.perf_counter() - t0
+    flops = 2.5 * acc.fwd_flops(1, 1, w["N"], w["d"], True) * len(heads)
+    return flops / sec / 1e12, sec
+
+
+CPU_HEADS = [(0, 0), (0, 8), (1, 3)]
+_CPU_INPUTS = {}
+
+
+def run_reference(args):
+    """The float64 CPU oracle timed on the host cores: each step is forward +
+    backward of one (b, h) head of the long workload (rotating over the 32
+    heads), reported in the same unit as the GPU arm."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    import synth  # noqa: F401  (inputs are generated inside cpu_sample)
+
+    heads = [(b, h) for b in range(LONG["B"]) for h in range(LONG["H"])]
+    for i in range(max(1, args.warmup)):
+        cpu_sample([heads[i % len(heads)]])
+    t0 = time.perf_counter()
+    tfs = []
+    for i in range(args.steps):
+        tf, _ = cpu_sample([heads[(args.warmup + i) % len(heads)]])
+        tfs.append(tf)
+    sec = time.perf_counter() - t0
+    value = len(tfs) / sum(1.0 / t for t in tfs)  # total work / total time
+    sample = f"one (b, h) head per step of the long workload, forward + backward in float64 ({args.steps} steps)"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * sec / args.steps, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "long: B=2 H=16 N=8192 d=128 causal, K x3 in heads 0-7",
+                   "flops_convention": "fwd 4BHN^2d/2; fwd+bwd 2.5x fwd", "sample": sample},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": N_CORES, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    rank, world, _ = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    import torch
+    import torch.distributed as dist
+
+    res, ctx = run_ours(args)
+    e2e = run_e2e(args, ctx)
+    if world > 1:
+        t = torch.tensor([e2e["ms_per_step"]], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e["value"] = round(world * float(e2e["value"]) * e2e["ms_per_step"] / float(t.item()), 2)
+        e2e["ms_per_step"] = round(float(t.item()), 4)
+    res["e2e"] = e2e
+    del ctx
+    torch.cuda.empty_cache()
+    if rank == 0 and world == 1 and not args.no_extra:
+        res["extra"] = run_extra(load_peaks())
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tf, sec = cpu_sample(CPU_HEADS)
+        res["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": N_CORES, "kind": "oracle",
+                               "sample": f"{len(CPU_HEADS)} of 32 (b, h) heads of the long workload, forward + "
+                                         f"backward in float64, {sec:.1f} s"}
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -21,7 +21,7 @@ namespace {
 
 struct Options {
   float tau = 8.0f;
-  bool poly = true;
+  bool poly = false;
   unsigned long long timeout_ns = 2000000000ull;
 } g_opt;
 
@@ -124,7 +124,7 @@ static fa_status fwd_common(const void* q, const void* k, const void* v, void* o
   if (!scale_ok(scale) || (causal != 0 && causal != 1)) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_MISALIGNED;
-  if ((long long)nbatch * H > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  if ((long long)nbatch * H > 65535LL * 8) return FA_ERR_INVALID_ARG;  // grid.z limit with 8-head groups
   const int num_pairs = (max_len + 255) / 256;
   if (num_pairs > 65535) return FA_ERR_INVALID_ARG;
   if (!ensure_init()) return FA_ERR_LAUNCH;
@@ -138,6 +138,7 @@ static fa_status fwd_common(const void* q, const void* k, const void* v, void* o
   p.lse = lse;
   p.cu_seqlens = cu;
   p.H = H;
+  p.bh_total = nbatch * H;
   p.n_rows = n_rows;
   p.seq_len = seq_len;
   p.num_pairs = num_pairs;

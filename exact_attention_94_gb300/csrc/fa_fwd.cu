@@ -62,6 +62,7 @@ struct FwdLayout {
 };
 
 constexpr int kThreads = 384;
+constexpr int kHeadGroup = 8;  // heads whose CTAs are scheduled together
 
 }  // namespace
 
@@ -84,8 +85,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = lane_id();
 
   // ---------------------------------------------------------------- work item
-  const int b = blockIdx.x / p.H;
-  const int h = blockIdx.x % p.H;
+  // grid: x = head within a group, y = query-tile pair (heaviest first), z = group of heads.
+  // The block scheduler walks x fastest, so the CTAs in flight share a few heads' K/V in L2.
+  const int bh = (int)(blockIdx.z * gridDim.x + blockIdx.x);
+  if (bh >= p.bh_total) return;
+  const int b = bh / p.H;
+  const int h = bh % p.H;
   const int pair = p.num_pairs - 1 - (int)blockIdx.y;  // heaviest causal pairs first
   int seq_start = 0, seq_len = p.seq_len, b_coord = b;
   if (p.cu_seqlens != nullptr) {
@@ -299,9 +304,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 128; ++i)
           if (kv0 + i >= lim) x[i] = -INFINITY;
       }
-      float mx = x[0];
+      // row maximum: eight short chains of 3-input maxima, then a small tree
+      float mg[8];
 #pragma unroll
-      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, x[i]);
+      for (int g = 0; g < 8; ++g) {
+        float m = fmaxf(x[16 * g], x[16 * g + 1]);
+#pragma unroll
+        for (int i = 2; i < 16; i += 2) m = max3f(m, x[16 * g + i], x[16 * g + i + 1]);
+        mg[g] = m;
+      }
+      const float mx = max3f(max3f(mg[0], mg[1], mg[2]), max3f(mg[3], mg[4], mg[5]), fmaxf(mg[6], mg[7]));
       const float m_new = mx * sl2;
       float alpha = 1.f;
       const bool resc = m_new > m_ref + tau;
@@ -311,23 +323,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
 
+      // p = 2^(x * scale * log2 e - m_ref): packed FMA, exponentials, packed partial sums
+      const uint64_t sl2x2 = f2_pack(sl2, sl2);
+      const uint64_t nmb2 = f2_pack(-mb, -mb);
+      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
       uint32_t pk[2][32];
-      float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
+        float y0, y1;
+        f2_unpack(f2_fma(f2_pack(x[2 * i], x[2 * i + 1]), sl2x2, nmb2), y0, y1);
         float p0, p1;
-        if (POLY && (i & 3) == 3) {
-          p0 = ex2_poly(fmaf(x[2 * i], sl2, -mb));
-          p1 = ex2_poly(fmaf(x[2 * i + 1], sl2, -mb));
+        if (POLY && (i & 7) == 7) {
+          p0 = ex2_poly(y0);
+          p1 = ex2_poly(y1);
         } else {
-          p0 = ex2_sfu(fmaf(x[2 * i], sl2, -mb));
-          p1 = ex2_sfu(fmaf(x[2 * i + 1], sl2, -mb));
+          p0 = ex2_sfu(y0);
+          p1 = ex2_sfu(y1);
         }
-        sum0 += p0;
-        sum1 += p1;
+        acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
         pk[i / 32][i % 32] = pack_bf16x2(p0, p1);
+        if (i == 31) tmem_st32(tS, pk[0]);  // first half of P out early: frees registers
       }
-      l = l * alpha + (sum0 + sum1);
+      float s0, s1, s2, s3, s4, s5, s6, s7;
+      f2_unpack(acc[0], s0, s1);
+      f2_unpack(acc[1], s2, s3);
+      f2_unpack(acc[2], s4, s5);
+      f2_unpack(acc[3], s6, s7);
+      l = l * alpha + (((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7)));
 
       if (j > 0 && __any_sync(0xffffffffu, resc)) {
         // rows whose reference moved: O~ *= alpha (alpha = 1 for the others)
@@ -341,7 +363,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(tO + 32 * c, ov);
         }
       }
-      tmem_st32(tS, pk[0]);
       tmem_st32(tS + 32, pk[1]);
       tmem_st_wait();
       tc_fence_before();
@@ -400,7 +421,8 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  dim3 grid(grid_x, p.num_pairs);
+  const int gx = grid_x < kHeadGroup ? grid_x : kHeadGroup;
+  dim3 grid(gx, p.num_pairs, (grid_x + gx - 1) / gx);
   kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }

@@ -14,6 +14,7 @@ struct FwdParams {
   float* lse;                // fp32 log-sum-exp
   const int* cu_seqlens;     // packed batch offsets (device) or nullptr for a dense batch
   int H;
+  int bh_total;              // (batch or sequences) * H
   int n_rows;                // rows along the sequence axis of the tensors (N, or total tokens)
   int seq_len;               // dense: N
   int num_pairs;             // grid.y: pairs of 128-row query tiles per (sequence, head)
