@@ -161,31 +161,89 @@ fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, fl
                         int num_seqs, int max_seqlen, int total_tokens, int H, int d, int causal, float scale,
                         fa_stream_t stream) {
   if (num_seqs < 1 || H < 1 || max_seqlen < 0 || total_tokens < 0 || !cu_seqlens) return FA_ERR_INVALID_ARG;
-  if (!aligned16(cu_seqlens) && ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0)) return FA_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0) return FA_ERR_MISALIGNED;
   if (total_tokens == 0 || max_seqlen == 0) return FA_OK;
   return fwd_common(q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, 0, max_seqlen, H, d, causal, scale,
                     stream);
 }
 
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 0 || d < 1) return 0;
-  const size_t acc = (size_t)B * N * H * d * sizeof(float);
-  const size_t rows = (size_t)B * H * N * sizeof(float);
-  return ((acc + 255) & ~(size_t)255) + ((rows + 255) & ~(size_t)255);
+  const size_t acc = (size_t)B * N * H * d * sizeof(float);  // fp32 dQ accumulator
+  const size_t rows = (size_t)B * H * N * sizeof(float);     // D and lse * log2 e
+  return align256(acc) + 2 * align256(rows);
 }
 
 size_t fa_bwd_varlen_workspace_bytes(int total_tokens, int H, int d) {
   return fa_bwd_workspace_bytes(1, H, total_tokens, d);
 }
 
-fa_status fa_bwd(const void*, const void*, const void*, const void*, const float*, const void*, void*, void*,
-                 void*, void*, int, int, int, int, int, float, fa_stream_t) {
-  return FA_ERR_UNSUPPORTED;
+static fa_status bwd_common(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                            const void* dout, void* dq, void* dk, void* dv, void* workspace, const int* cu,
+                            int nbatch, int n_rows, int seq_len, int max_len, int H, int d, int causal,
+                            float scale, fa_stream_t stream) {
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (!scale_ok(scale) || (causal != 0 && causal != 1)) return FA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv, workspace};
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) return FA_ERR_MISALIGNED;
+  if ((long long)nbatch * H > 65535LL * 8) return FA_ERR_INVALID_ARG;
+  const int num_kblocks = (max_len + 127) / 128;
+  if (num_kblocks > 65535) return FA_ERR_INVALID_ARG;
+  if (!ensure_init()) return FA_ERR_LAUNCH;
+  const int tb = cu ? 1 : nbatch;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_tmap_bhnd(&tq, q, d, n_rows, H, tb) || !make_tmap_bhnd(&tk, k, d, n_rows, H, tb) ||
+      !make_tmap_bhnd(&tv, v, d, n_rows, H, tb) || !make_tmap_bhnd(&tdo, dout, d, n_rows, H, tb))
+    return FA_ERR_INVALID_ARG;
+  const size_t acc_bytes = align256((size_t)tb * n_rows * H * d * sizeof(float));
+  const size_t row_bytes = align256((size_t)tb * H * n_rows * sizeof(float));
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  BwdParams p{};
+  p.o = o;
+  p.dout = dout;
+  p.lse = lse;
+  p.dq_acc = reinterpret_cast<float*>(ws);
+  p.dsum = reinterpret_cast<float*>(ws + acc_bytes);
+  p.lse2 = reinterpret_cast<float*>(ws + acc_bytes + row_bytes);
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.cu_seqlens = cu;
+  p.B = nbatch;
+  p.B_tensor = tb;
+  p.H = H;
+  p.n_rows = n_rows;
+  p.seq_len = seq_len;
+  p.num_kblocks = num_kblocks;
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  p.err = g_err_ptr;
+  p.timeout_ns = g_opt.timeout_ns;
+  cudaError_t e = launch_bwd(tq, tk, tv, tdo, p, d, causal != 0, (cudaStream_t)stream);
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
-fa_status fa_bwd_varlen(const void*, const void*, const void*, const void*, const float*, const void*, void*, void*,
-                        void*, void*, const int*, int, int, int, int, int, int, float, fa_stream_t) {
-  return FA_ERR_UNSUPPORTED;
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                 void* dq, void* dk, void* dv, void* workspace, int B, int H, int N, int d, int causal, float scale,
+                 fa_stream_t stream) {
+  if (B < 1 || H < 1 || N < 0) return FA_ERR_INVALID_ARG;
+  if (N == 0) return FA_OK;
+  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, nullptr, B, N, N, N, H, d, causal, scale, stream);
+}
+
+fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                        const void* dout, void* dq, void* dk, void* dv, void* workspace, const int* cu_seqlens,
+                        int num_seqs, int max_seqlen, int total_tokens, int H, int d, int causal, float scale,
+                        fa_stream_t stream) {
+  if (num_seqs < 1 || H < 1 || max_seqlen < 0 || total_tokens < 0 || !cu_seqlens) return FA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0) return FA_ERR_MISALIGNED;
+  if (total_tokens == 0 || max_seqlen == 0) return FA_OK;
+  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, cu_seqlens, num_seqs, total_tokens, 0,
+                    max_seqlen, H, d, causal, scale, stream);
 }
 
 size_t fa_decode_workspace_bytes(int B, int H, int d, int num_splits) {

@@ -1,2 +1,486 @@
-// Backward kernels (filled in below the forward path).
+// Backward kernels: gradients of exact attention by recomputation.
+//
+// Method ("13.14 FlashAttention: IO-aware exact attention", "Backpropagation
+// uses the same trick": tiles of P are recomputed instead of stored;
+// FlashAttention-2 in "efficient-attention/flash-2-3": each weight is
+// recomputed as e^(s - lse), the backward is parallel over key blocks, and
+// many blocks add into the same dQ_i with atomic additions):
+//
+//   pre:   D_i = sum_c dO_ic O_ic;  lse2_i = lse_i * log2 e;  dQacc = 0
+//   main:  one CTA per 128-key block K_j, V_j; for every query block i
+//          (i >= j when causal):
+//            S^T  = K_j Q_i^T                 (tcgen05, TMEM)
+//            dP^T = V_j dO_i^T                (tcgen05, TMEM)
+//            P^T  = 2^(S^T scale log2 e - lse2)       (bf16, back into TMEM)
+//            dS^T = scale * P^T * (dP^T - D)          (bf16, shared memory)
+//            dV_j += P^T dO_i;  dK_j += dS^T Q_i      (tcgen05, TMEM accumulators)
+//            dQ_i  = dS K_j  -> added into dQacc with vector atomics
+//   post:  dQ = bf16(dQacc)
+//
+// The fp32 dQ accumulator is laid out [B*H][d/4][rows][4]: a warp's 32
+// threads (32 consecutive query rows) add one 4-float group each, so every
+// warp-wide atomic covers 512 contiguous bytes.
+//
+// CTA roles (384 threads): warp 0 TMA producer, warp 1 TMEM owner and MMA
+// issuer, warps 4-7 recompute P and dS (thread = key row = TMEM lane),
+// warps 8-11 drain dQ tiles from TMEM into the accumulator (thread = query
+// row).  TMEM: S^T/P^T [0,128), dP^T/dQ [128,256), dV [256,256+d),
+// dK [256+d,256+2d).
 #include "fa_internal.h"
+#include "ptx.cuh"
+
+#include <cmath>
+
+namespace fa {
+
+namespace {
+
+constexpr int kBwdThreads = 384;
+constexpr int kBwdHeadGroup = 8;
+
+template <int D>
+struct BwdLayout {
+  static constexpr uint32_t kTile = 128u * D * 2u;  // one 128-row bf16 tile
+  static constexpr uint32_t kChunk = 128u * 128u;   // 128 rows x 128 bytes
+  static constexpr uint32_t kK = 0;
+  static constexpr uint32_t kV = kTile;
+  static constexpr uint32_t kStage0 = 2 * kTile;     // stage s: Q_i then dO_i
+  static constexpr uint32_t kStageBytes = 2 * kTile;
+  static constexpr uint32_t kDS = kStage0 + 2 * kStageBytes;  // 128 x 128 bf16, two 64-column chunks
+  static constexpr uint32_t kBar = kDS + 2 * kChunk;
+  static constexpr uint32_t kBytes = kBar + 128 + 1024 + 1024;  // barriers, lse2/D rows, alignment slack
+};
+
+}  // namespace
+
+// ---------------------------------------------------------------- pre / post
+
+// One warp per row (b, h, n): D = sum_c dO * O, lse2 = lse * log2 e; the
+// dQ accumulator rows it owns are zeroed.  Tensors [Bt][rows][H][d].
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
+                                                        const __nv_bfloat16* __restrict__ dout,
+                                                        const float* __restrict__ lse, float* __restrict__ dsum,
+                                                        float* __restrict__ lse2, float* __restrict__ dq_acc,
+                                                        int H, int n_rows, long long total_rows) {
+  const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (gw >= total_rows) return;
+  // gw enumerates (bt, h, n) with n fastest
+  const int n = (int)(gw % n_rows);
+  const long long bh = gw / n_rows;
+  const int h = (int)(bh % H);
+  const long long bt = bh / H;
+  const size_t base = (((size_t)bt * n_rows + n) * H + h) * D;
+  constexpr int PER = D / 32;  // elements per lane
+  float acc = 0.f;
+  if constexpr (PER == 4) {
+    const uint2 a = *reinterpret_cast<const uint2*>(o + base + lane * 4);
+    const uint2 b = *reinterpret_cast<const uint2*>(dout + base + lane * 4);
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float2 fa = __bfloat1622float2(a2[i]);
+      const float2 fb = __bfloat1622float2(b2[i]);
+      acc = fmaf(fa.x, fb.x, fmaf(fa.y, fb.y, acc));
+    }
+  } else {
+    const uint32_t a = *reinterpret_cast<const uint32_t*>(o + base + lane * 2);
+    const uint32_t b = *reinterpret_cast<const uint32_t*>(dout + base + lane * 2);
+    const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a));
+    const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b));
+    acc = fmaf(fa.x, fb.x, fa.y * fb.y);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  const size_t ri = (size_t)bh * n_rows + n;
+  if (lane == 0) {
+    dsum[ri] = acc;
+    lse2[ri] = lse[ri] * 1.4426950408889634f;
+  }
+  // zero this row of the accumulator: d/4 groups of 4 floats
+  if (lane < D / 4) {
+    float4* dst = reinterpret_cast<float4*>(dq_acc) + ((size_t)bh * (D / 4) + lane) * n_rows + n;
+    *dst = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// dq[bt][n][h][c] = bf16(acc[bt*H+h][c/4][n][c%4]); one thread per 4 columns of a row.
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_post_kernel(const float* __restrict__ dq_acc,
+                                                         __nv_bfloat16* __restrict__ dq, int H, int n_rows,
+                                                         long long total) {
+  const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= total) return;
+  // t enumerates (bt, n, h, c4) with c4 fastest: coalesced bf16 writes
+  constexpr int G = D / 4;
+  const int c4 = (int)(t % G);
+  long long r = t / G;
+  const int h = (int)(r % H);
+  r /= H;
+  const int n = (int)(r % n_rows);
+  const long long bt = r / n_rows;
+  const long long bh = bt * H + h;
+  const float4 v = reinterpret_cast<const float4*>(dq_acc)[((size_t)bh * G + c4) * n_rows + n];
+  uint2 out;
+  out.x = pack_bf16x2(v.x, v.y);
+  out.y = pack_bf16x2(v.z, v.w);
+  *reinterpret_cast<uint2*>(dq + (((size_t)bt * n_rows + n) * H + h) * D + c4 * 4) = out;
+}
+
+// ---------------------------------------------------------------- main
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                       const BwdParams p) {
+  using L = BwdLayout<D>;
+  constexpr int CH = D / 64;
+  constexpr uint32_t TILE = L::kTile;
+  constexpr uint32_t CHUNK = L::kChunk;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sbase = smem_raw + (base - raw);
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+
+  // ---------------------------------------------------------------- work item
+  const int bh = (int)(blockIdx.z * gridDim.x + blockIdx.x);
+  if (bh >= p.B * p.H) return;
+  const int b = bh / p.H;
+  const int h = bh % p.H;
+  const int jb = (int)blockIdx.y;  // key block; ascending = heaviest first when causal
+  int seq_start = 0, seq_len = p.seq_len, b_coord = b;
+  if (p.cu_seqlens != nullptr) {
+    seq_start = p.cu_seqlens[b];
+    seq_len = p.cu_seqlens[b + 1] - seq_start;
+    b_coord = 0;
+  }
+  const int k0 = jb * 128;
+  if (k0 >= seq_len) return;
+  const int n_qblk = (seq_len + 127) / 128;
+  const int i_begin = CAUSAL ? jb : 0;
+  const int n_steps = n_qblk - i_begin;
+  const size_t row_base = (size_t)(b_coord * p.H + h) * p.n_rows + seq_start;  // lse2 / dsum / acc row origin
+
+  // ---------------------------------------------------------------- barriers
+  enum { KV_FULL = 0, Q_FULL = 1, STAGE_EMPTY = 3, S_FULL = 5, DP_FULL, P_READY, DQ_FULL, DQ_EMPTY, DS_EMPTY,
+         DKV_FINAL, DRAIN, NBARS };
+  const uint32_t bar0 = base + L::kBar;
+  auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + L::kBar + 8 * NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* s_lse2 = reinterpret_cast<float*>(sbase + L::kBar + 128);  // 128 floats
+  float* s_dsum = s_lse2 + 128;                                     // 128 floats
+
+  if (threadIdx.x == 0) {
+    mbar_init(BAR(KV_FULL), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(BAR(Q_FULL + s), 1);
+      mbar_init(BAR(STAGE_EMPTY + s), 1);
+    }
+    mbar_init(BAR(S_FULL), 1);
+    mbar_init(BAR(DP_FULL), 1);
+    mbar_init(BAR(P_READY), 128);
+    mbar_init(BAR(DQ_FULL), 1);
+    mbar_init(BAR(DQ_EMPTY), 128);
+    mbar_init(BAR(DS_EMPTY), 1);
+    mbar_init(BAR(DKV_FINAL), 1);
+    mbar_init(BAR(DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtx w{abort_flag, p.timeout_ns, p.err};
+
+  const uint32_t sK = base + L::kK, sV = base + L::kV, sDS = base + L::kDS;
+  auto stage_q = [&](int st) -> uint32_t { return base + L::kStage0 + (uint32_t)st * L::kStageBytes; };
+
+  if (warp == 0) {
+    // ============================================================ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      mbar_arrive_expect_tx(BAR(KV_FULL), 2 * TILE);
+      for (int c = 0; c < CH; ++c) {
+        tma_load_4d(sK + c * CHUNK, &tm_k, BAR(KV_FULL), c * 64, seq_start + k0, h, b_coord);
+        tma_load_4d(sV + c * CHUNK, &tm_v, BAR(KV_FULL), c * 64, seq_start + k0, h, b_coord);
+      }
+      bool ok = true;
+      for (int n = 0; n < n_steps && ok; ++n) {
+        const int st = n & 1;
+        const int row = seq_start + (i_begin + n) * 128;
+        if (n >= 2 && !(ok = mbar_wait(BAR(STAGE_EMPTY + st), ((n >> 1) - 1) & 1, w, 21))) break;
+        mbar_arrive_expect_tx(BAR(Q_FULL + st), 2 * TILE);
+        const uint32_t qa = stage_q(st);
+        for (int c = 0; c < CH; ++c) {
+          tma_load_4d(qa + c * CHUNK, &tm_q, BAR(Q_FULL + st), c * 64, row, h, b_coord);
+          tma_load_4d(qa + TILE + c * CHUNK, &tm_do, BAR(Q_FULL + st), c * 64, row, h, b_coord);
+        }
+      }
+      if (!ok) {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 200000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ============================================================ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_ST = idesc_bf16(128, 128, false, false);  // S^T, dP^T
+      constexpr uint32_t IDESC_KV = idesc_bf16(128, D, false, true);     // dV, dK
+      constexpr uint32_t IDESC_Q = idesc_bf16(128, D, true, true);       // dQ
+      const uint32_t tS = tmem, tDP = tmem + 128, tDV = tmem + 256, tDK = tmem + 256 + D;
+      bool ok = mbar_wait(BAR(KV_FULL), 0, w, 22);
+      tc_fence_after();
+      for (int n = 0; n < n_steps && ok; ++n) {
+        const int st = n & 1;
+        const uint32_t qa = stage_q(st), da = qa + TILE;
+        if (!(ok = mbar_wait(BAR(Q_FULL + st), (n >> 1) & 1, w, 23))) break;
+        tc_fence_after();
+        // S^T = K_j Q_i^T   (M = keys, N = queries, K = d; both K-major)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * CHUNK + (kk % 4) * 32;
+          mma_ss(tS, smem_desc_sw128(sK + off, 16, 1024), smem_desc_sw128(qa + off, 16, 1024), IDESC_ST, kk > 0);
+        }
+        mma_commit(BAR(S_FULL));
+        if (n > 0) {
+          if (!(ok = mbar_wait(BAR(DQ_EMPTY), (n - 1) & 1, w, 24))) break;
+          tc_fence_after();
+        }
+        // dP^T = V_j dO_i^T
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * CHUNK + (kk % 4) * 32;
+          mma_ss(tDP, smem_desc_sw128(sV + off, 16, 1024), smem_desc_sw128(da + off, 16, 1024), IDESC_ST, kk > 0);
+        }
+        mma_commit(BAR(DP_FULL));
+        if (!(ok = mbar_wait(BAR(P_READY), n & 1, w, 25))) break;
+        tc_fence_after();
+        // dV += P^T dO_i   (A = P^T from TMEM, B = dO_i MN-major; K = 128 queries)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tDV, tS + kk * 8, smem_desc_sw128(da + kk * 2048, CHUNK, 1024), IDESC_KV, (n > 0 || kk > 0) ? 1u : 0u);
+        // dK += dS^T Q_i   (A = dS^T K-major in shared memory, B = Q_i MN-major)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tDK, smem_desc_sw128(sDS + (kk / 4) * CHUNK + (kk % 4) * 32, 16, 1024),
+                 smem_desc_sw128(qa + kk * 2048, CHUNK, 1024), IDESC_KV, (n > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(BAR(STAGE_EMPTY + st));
+        // dQ_i = dS K_j   (M = queries: A = dS MN-major over the same buffer, B = K_j MN-major; K = 128 keys)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tDP, smem_desc_sw128(sDS + kk * 2048, CHUNK, 1024), smem_desc_sw128(sK + kk * 2048, CHUNK, 1024),
+                 IDESC_Q, kk > 0);
+        mma_commit(BAR(DQ_FULL));
+        mma_commit(BAR(DS_EMPTY));
+      }
+      if (ok) mma_commit(BAR(DKV_FINAL));
+      mma_commit(BAR(DRAIN));
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(BAR(DRAIN), 0) && globaltimer_ns() - t0 < p.timeout_ns) {
+      }
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ============================================================ P and dS (thread = key row)
+    const int kw = warp & 3;
+    const int kr = kw * 32 + lane;
+    const int kg = k0 + kr;
+    const bool row_ok = kg < seq_len;
+    const uint32_t lane_off = (uint32_t)(kw * 32) << 16;
+    const uint32_t tS = tmem + lane_off, tDP = tmem + lane_off + 128;
+    const float sl2 = p.scale_log2;
+    const float scale = p.scale;
+    const int swz = kr & 7;
+    uint8_t* ds_row = sbase + L::kDS + kr * 128;
+    bool ok = true;
+    for (int n = 0; n < n_steps; ++n) {
+      const int q0 = (i_begin + n) * 128;
+      // stage this query block's lse2 and D (invalid rows: lse2 = +inf, so P = 0)
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      {
+        const int qg = q0 + kr;
+        const bool qv = qg < seq_len;
+        s_lse2[kr] = qv ? p.lse2[row_base + qg] : INFINITY;
+        s_dsum[kr] = qv ? p.dsum[row_base + qg] : 0.f;
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      // After an abort the warp keeps taking part in the two named barriers of every
+      // step (so the other warps of the group never wait on it) and does nothing else.
+      if (!ok) continue;
+      ok = mbar_wait(BAR(S_FULL), n & 1, w, 26) && mbar_wait(BAR(DP_FULL), n & 1, w, 27) &&
+           (n == 0 || mbar_wait(BAR(DS_EMPTY), (n - 1) & 1, w, 28));
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        continue;
+      }
+      tc_fence_after();
+      const bool diag = CAUSAL && (q0 == k0);
+#pragma unroll 2
+      for (int c = 0; c < 8; ++c) {
+        uint32_t sr[16], dr[16];
+        tmem_ld16(tS + 16 * c, sr);
+        tmem_ld16(tDP + 16 * c, dr);
+        tmem_ld_wait();
+        const float4* l4 = reinterpret_cast<const float4*>(s_lse2 + 16 * c);
+        const float4* d4 = reinterpret_cast<const float4*>(s_dsum + 16 * c);
+        float lv[16], dv[16];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const float4 a = l4[g], bq = d4[g];
+          lv[4 * g] = a.x; lv[4 * g + 1] = a.y; lv[4 * g + 2] = a.z; lv[4 * g + 3] = a.w;
+          dv[4 * g] = bq.x; dv[4 * g + 1] = bq.y; dv[4 * g + 2] = bq.z; dv[4 * g + 3] = bq.w;
+        }
+        uint32_t pp[8], dd[8];
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) {
+          float p0 = ex2_sfu(fmaf(__uint_as_float(sr[e]), sl2, -lv[e]));
+          float p1 = ex2_sfu(fmaf(__uint_as_float(sr[e + 1]), sl2, -lv[e + 1]));
+          if (!row_ok) {
+            p0 = 0.f;
+            p1 = 0.f;
+          }
+          if (diag) {
+            const int qg = q0 + 16 * c + e;
+            if (kg > qg) p0 = 0.f;
+            if (kg > qg + 1) p1 = 0.f;
+          }
+          const float g0 = p0 * scale * (__uint_as_float(dr[e]) - dv[e]);
+          const float g1 = p1 * scale * (__uint_as_float(dr[e + 1]) - dv[e + 1]);
+          pp[e / 2] = pack_bf16x2(p0, p1);
+          dd[e / 2] = pack_bf16x2(g0, g1);
+        }
+        tmem_st8(tS + 8 * c, pp);  // P^T over already-consumed S^T columns
+        // dS^T row kr, queries 16c..16c+15: 128-byte swizzled K-major layout
+        const int unit = 2 * (c & 3);
+        uint8_t* chunk = ds_row + (c >> 2) * CHUNK;
+        *reinterpret_cast<uint4*>(chunk + ((unit ^ swz) << 4)) = make_uint4(dd[0], dd[1], dd[2], dd[3]);
+        *reinterpret_cast<uint4*>(chunk + (((unit + 1) ^ swz) << 4)) = make_uint4(dd[4], dd[5], dd[6], dd[7]);
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(BAR(P_READY));
+    }
+    // ------------------------------------------------------------ dK, dV epilogue
+    if (ok) {
+      ok = mbar_wait(BAR(DKV_FINAL), 0, w, 29);
+      if (__all_sync(0xffffffffu, ok)) {
+        tc_fence_after();
+        const size_t grow = ((size_t)b_coord * p.n_rows + seq_start + kg) * p.H + h;
+        __nv_bfloat16* dv_row = reinterpret_cast<__nv_bfloat16*>(p.dv) + grow * D;
+        __nv_bfloat16* dk_row = reinterpret_cast<__nv_bfloat16*>(p.dk) + grow * D;
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          const uint32_t src = tmem + lane_off + 256 + (which ? (uint32_t)D : 0u);
+          __nv_bfloat16* dst = which ? dk_row : dv_row;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(src + 32 * c, v);
+            tmem_ld_wait();
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+            if (row_ok) {
+              uint4* o4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) o4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
+          }
+        }
+      }
+    }
+  } else if (warp >= 8) {
+    // ============================================================ dQ drain (thread = query row)
+    const int qw = warp & 3;
+    const int r = qw * 32 + lane;
+    const uint32_t tDQ = tmem + ((uint32_t)(qw * 32) << 16) + 128;
+    float4* acc = reinterpret_cast<float4*>(p.dq_acc) + (size_t)(b_coord * p.H + h) * (D / 4) * p.n_rows;
+    for (int n = 0; n < n_steps; ++n) {
+      const int qg = (i_begin + n) * 128 + r;
+      bool ok = mbar_wait(BAR(DQ_FULL), n & 1, w, 30);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      uint32_t v[D];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(tDQ + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(BAR(DQ_EMPTY));  // TMEM free for the next dP^T while the adds go out
+      if (qg < seq_len) {
+        const size_t row = (size_t)seq_start + qg;
+#pragma unroll
+        for (int g = 0; g < D / 4; ++g)
+          atomicAdd(acc + (size_t)g * p.n_rows + row,
+                    make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
+                                __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3])));
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool CAUSAL>
+static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream) {
+  const long long rows = (long long)p.B_tensor * p.H * p.n_rows;
+  fa_bwd_pre_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(p.o), static_cast<const __nv_bfloat16*>(p.dout), p.lse, p.dsum, p.lse2,
+      p.dq_acc, p.H, p.n_rows, rows);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  auto kern = fa_bwd_main_kernel<D, CAUSAL>;
+  constexpr uint32_t smem = BwdLayout<D>::kBytes;
+  static bool configured = false;
+  if (!configured) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int bh = p.B * p.H;
+  const int gx = bh < kBwdHeadGroup ? bh : kBwdHeadGroup;
+  dim3 grid(gx, p.num_kblocks, (bh + gx - 1) / gx);
+  kern<<<grid, kBwdThreads, smem, stream>>>(tq, tk, tv, tdo, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  const long long total = rows * (D / 4);
+  fa_bwd_post_kernel<D><<<(unsigned)((total + 255) / 256), 256, 0, stream>>>(
+      p.dq_acc, static_cast<__nv_bfloat16*>(p.dq), p.H, p.n_rows, total);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                       const BwdParams& p, int D, bool causal, cudaStream_t stream) {
+  if (D == 64) return causal ? launch_bwd_t<64, true>(tq, tk, tv, tdo, p, stream)
+                             : launch_bwd_t<64, false>(tq, tk, tv, tdo, p, stream);
+  if (D == 128) return causal ? launch_bwd_t<128, true>(tq, tk, tv, tdo, p, stream)
+                              : launch_bwd_t<128, false>(tq, tk, tv, tdo, p, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

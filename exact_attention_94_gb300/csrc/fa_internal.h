@@ -25,22 +25,21 @@ struct FwdParams {
 };
 
 struct BwdParams {
-  const void* q;
-  const void* k;
-  const void* v;
   const void* o;
   const void* dout;
-  const float* lse;
-  float* dsum;               // D_i, [B, H, N] / [H, total]
-  float* dq_acc;             // fp32 accumulator, same layout as q
+  const float* lse;          // natural-log lse from the forward
+  float* lse2;               // workspace: lse * log2 e, same layout as lse
+  float* dsum;               // workspace: D_i = sum_c dO_ic O_ic, same layout as lse
+  float* dq_acc;             // workspace: fp32 [B_tensor*H][d/4][n_rows][4]
   void* dq;
   void* dk;
   void* dv;
-  const int* cu_seqlens;
+  const int* cu_seqlens;     // packed batch offsets (device) or nullptr
   int B;                     // dense batch, or number of sequences
+  int B_tensor;              // leading extent of the tensors: B (dense) or 1 (packed)
   int H;
-  int n_rows;
-  int seq_len;
+  int n_rows;                // rows along the sequence axis of the tensors
+  int seq_len;               // dense: N
   int num_kblocks;           // grid.y of the main kernel
   float scale;
   float scale_log2;
@@ -56,8 +55,7 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                        int D, bool causal, bool poly, int grid_x, cudaStream_t stream);
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const BwdParams& p, int D, bool causal, int grid_x,
-                       cudaStream_t stream);
+                       const CUtensorMap& tdo, const BwdParams& p, int D, bool causal, cudaStream_t stream);
 
 cudaError_t launch_decode(const void* q, const void* k, const void* v, void* o, float* lse, float* part_o,
                           float* part_lse, int B, int H, int L, int D, int num_splits, float scale_log2,
