@@ -7,7 +7,9 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libfa.so")
 
-FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_MISALIGNED, FA_ERR_LAUNCH, FA_ERR_TIMEOUT = range(6)
+(FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_MISALIGNED, FA_ERR_LAUNCH, FA_ERR_TIMEOUT,
+ FA_ERR_SCRATCH_LIMIT) = range(7)
+FA_BWD_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 FA_OPT_RESCALE_TAU, FA_OPT_POLY_EXP, FA_OPT_WAIT_TIMEOUT_MS = 1, 2, 3
 
 # every symbol include/fa.h declares, with (restype, argtypes)
@@ -22,6 +24,7 @@ SIGNATURES = {
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "fa_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "fa_bwd_varlen_workspace_bytes": (_S, [_I, _I, _I]),
+    "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "fa_bwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "fa_decode_workspace_bytes": (_S, [_I, _I, _I, _I]),
     "fa_decode_num_splits": (_I, [_I, _I, _I, _I]),

@@ -81,6 +81,7 @@ const char* fa_status_string(fa_status s) {
     case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED";
     case FA_ERR_LAUNCH: return "FA_ERR_LAUNCH";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    case FA_ERR_SCRATCH_LIMIT: return "FA_ERR_SCRATCH_LIMIT";
   }
   return "FA_ERR_UNKNOWN";
 }
@@ -244,6 +245,46 @@ fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void*
   if (total_tokens == 0 || max_seqlen == 0) return FA_OK;
   return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, cu_seqlens, num_seqs, total_tokens, 0,
                     max_seqlen, H, d, causal, scale, stream);
+}
+
+// ---------------------------------------------------------------- backward without allocation
+//
+// Scratch of fa_bwd_noalloc: the fp32 dQ accumulator and the two per-row
+// arrays fa_bwd otherwise takes from a caller-allocated workspace.  It is
+// part of the library's device image, so every GPU that loads the library
+// holds these bytes until the process exits.  All calls share it.
+static __device__ __align__(256) unsigned char g_bwd_scratch[FA_BWD_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};  // device address of g_bwd_scratch, per device ordinal
+}  // namespace
+
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
+                         float scale, fa_stream_t stream) {
+  if (B < 1 || H < 1 || N < 0) return FA_ERR_INVALID_ARG;
+  if (N == 0) return FA_OK;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (fa_bwd_workspace_bytes(B, H, N, d) > (size_t)FA_BWD_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_LIMIT;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_LAUNCH;
+  void* scratch = nullptr;
+  {
+    // First call on this device: look up the array's device address with the
+    // device current (in host code the symbol itself is only a stand-in).
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (g_scratch_ptr[dev] == nullptr) {
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_bwd_scratch) != cudaSuccess || ptr == nullptr) return FA_ERR_LAUNCH;
+      g_scratch_ptr[dev] = ptr;
+    }
+    scratch = g_scratch_ptr[dev];
+  }
+  // The pre-kernel of the backward zeroes the accumulator part of the scratch
+  // and overwrites the per-row arrays, so the previous call's contents never leak.
+  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, scratch, nullptr, B, N, N, N, H, d, causal, scale, stream);
 }
 
 size_t fa_decode_workspace_bytes(int B, int H, int d, int num_splits) {

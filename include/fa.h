@@ -57,7 +57,8 @@ typedef enum {
   FA_ERR_UNSUPPORTED = 2, /* head dim not in {64, 128}, device not sm_103 */
   FA_ERR_MISALIGNED = 3,  /* a device pointer not 16-byte aligned */
   FA_ERR_LAUNCH = 4,      /* the CUDA runtime refused a launch */
-  FA_ERR_TIMEOUT = 5      /* a bounded wait inside a kernel ran out */
+  FA_ERR_TIMEOUT = 5,     /* a bounded wait inside a kernel ran out */
+  FA_ERR_SCRATCH_LIMIT = 6 /* fa_bwd_noalloc: the problem needs more than its built-in scratch */
 } fa_status;
 
 /* Human-readable name of a status code (static storage). */
@@ -121,6 +122,42 @@ fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void*
                         const void* dout, void* dq, void* dk, void* dv, void* workspace, const int* cu_seqlens,
                         int num_seqs, int max_seqlen, int total_tokens, int H, int d, int causal, float scale,
                         fa_stream_t stream);
+
+/*
+ * Size of the built-in scratch of fa_bwd_noalloc: 32 MiB of device memory,
+ * compiled into the library and held by every GPU that loads it until the
+ * process exits.
+ */
+#define FA_BWD_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * Backward pass for callers that cannot allocate device memory.  The pages
+ * have no counterpart: this is a library-interface variant of fa_bwd.
+ *
+ * Some callers may not call cudaMalloc or any allocating routine: code
+ * running inside a host-side memory budget with no allocator of its own, or a
+ * runtime that forbids allocation while it issues work.  This call takes the
+ * same inputs and outputs as fa_bwd (dense layout, caller-owned buffers) but
+ * no workspace: its scratch (the fp32 dQ accumulator and the per-row D and
+ * lse arrays, fa_bwd_workspace_bytes(B, H, N, d) bytes) lives in a fixed
+ * array inside the library.  It allocates nothing and calls no allocating
+ * routine.
+ *
+ *   Limit: fa_bwd_workspace_bytes(B, H, N, d) <= FA_BWD_NOALLOC_SCRATCH_BYTES
+ *          (for d = 128 about 64 K rows of B*H*N, for d = 64 about 125 K);
+ *          larger problems return FA_ERR_SCRATCH_LIMIT without launching.
+ *   Set-up: the first call on each device looks up the scratch array's device
+ *          address with that device current; make that first call before
+ *          any stream capture.
+ *   Sharing: every call on a device uses the same scratch.  The kernels clear
+ *          what must start at zero, but two calls whose work overlaps on the
+ *          GPU (different streams, or host threads racing) corrupt each
+ *          other's results: order them on one stream or synchronise.
+ * Other arguments and errors as fa_bwd.
+ */
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
+                         float scale, fa_stream_t stream);
 
 /*
  * Scratch bytes fa_decode_splitkv needs for num_splits partial results:
