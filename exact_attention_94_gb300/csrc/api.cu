@@ -294,16 +294,62 @@ size_t fa_decode_workspace_bytes(int B, int H, int d, int num_splits) {
   return ((po + 255) & ~(size_t)255) + ((pl + 255) & ~(size_t)255);
 }
 
-int fa_decode_num_splits(int B, int H, int L, int d) {
-  (void)B;
-  (void)H;
-  (void)d;
-  return L > 0 ? 1 : 0;
+// Heads handled by one decode CTA: the largest divisor of H that is at most 32.
+static int decode_group(int H) {
+  for (int g = H < 32 ? H : 32; g > 1; --g)
+    if (H % g == 0) return g;
+  return 1;
 }
 
-fa_status fa_decode_splitkv(const void*, const void*, const void*, void*, float*, int, int, int, int, int, void*,
-                            float, fa_stream_t) {
-  return FA_ERR_UNSUPPORTED;
+int fa_decode_num_splits(int B, int H, int L, int d) {
+  (void)d;
+  if (B < 1 || H < 1 || L <= 0) return 1;
+  int dev = 0, n_sm = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+  const long long ctas_per_split = (long long)B * (H / decode_group(H));
+  // about eight full waves of one CTA per SM, and at least 256 keys per split
+  long long s = (8LL * n_sm + ctas_per_split - 1) / ctas_per_split;
+  const long long max_s = (L + 255) / 256;
+  if (s > max_s) s = max_s;
+  if (s < 1) s = 1;
+  return (int)s;
+}
+
+fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse, int B,
+                            int H, int L, int d, int num_splits, void* workspace, float scale, fa_stream_t stream) {
+  if (!q || !o || !lse || !workspace) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || L < 0 || num_splits < 0) return FA_ERR_INVALID_ARG;
+  if (L > 0 && (!k_cache || !v_cache)) return FA_ERR_INVALID_ARG;  // an empty cache may be null
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k_cache, v_cache, o, lse, workspace};
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) return FA_ERR_MISALIGNED;
+  const int S = num_splits > 0 ? num_splits : fa_decode_num_splits(B, H, L, d);
+  if (L > 0 && S > L) return FA_ERR_INVALID_ARG;
+  const int G = decode_group(H);
+  if (B > 65535 || H / G > 65535) return FA_ERR_INVALID_ARG;
+  if (!ensure_init()) return FA_ERR_LAUNCH;
+  const size_t part_bytes = align256((size_t)B * H * S * d * sizeof(float));
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  DecodeParams p{};
+  p.q = q;
+  p.k = k_cache;
+  p.v = v_cache;
+  p.part_o = reinterpret_cast<float*>(ws);
+  p.part_lse = reinterpret_cast<float*>(ws + part_bytes);
+  p.B = B;
+  p.H = H;
+  p.L = L;
+  p.G = G;
+  p.chunk = L > 0 ? (L + S - 1) / S : 0;
+  p.num_splits = S;
+  p.stages = decode_stages(G, d);
+  p.scale_log2 = scale * kLog2e;
+  p.err = g_err_ptr;
+  p.timeout_ns = g_opt.timeout_ns;
+  cudaError_t e = launch_decode(p, d, o, lse, (cudaStream_t)stream);
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 }  // extern "C"

@@ -57,8 +57,26 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const BwdParams& p, int D, bool causal, cudaStream_t stream);
 
-cudaError_t launch_decode(const void* q, const void* k, const void* v, void* o, float* lse, float* part_o,
-                          float* part_lse, int B, int H, int L, int D, int num_splits, float scale_log2,
-                          cudaStream_t stream);
+struct DecodeParams {
+  const void* q;             // [B, 1, H, d] bf16
+  const void* k;             // [B, L, H, d] bf16
+  const void* v;
+  float* part_o;             // [B, H, num_splits, d] fp32: each chunk's normalised output
+  float* part_lse;           // [B, H, num_splits] fp32: each chunk's log2 softmax mass
+  int B;
+  int H;
+  int L;
+  int G;                     // heads per CTA (divides H, at most 32)
+  int chunk;                 // keys per split
+  int num_splits;
+  int stages;                // shared-memory ring depth
+  float scale_log2;
+  unsigned* err;
+  unsigned long long timeout_ns;
+};
+
+int decode_stages(int G, int D);
+size_t decode_smem_bytes(int G, int D);
+cudaError_t launch_decode(const DecodeParams& p, int D, void* o, float* lse, cudaStream_t stream);
 
 }  // namespace fa
