@@ -55,11 +55,11 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 }  // namespace
 
-bool make_tmap_bhnd(CUtensorMap* m, const void* ptr, int D, int n_rows, int H, int B) {
+bool make_tmap_bhnd(CUtensorMap* m, const void* ptr, int D, int n_rows, int H, int B, int box_rows) {
   const cuuint64_t e = 2;  // bytes per bf16
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)n_rows, (cuuint64_t)H, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)H * D * e, (cuuint64_t)D * e, (cuuint64_t)n_rows * H * D * e};
-  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -197,8 +197,9 @@ static fa_status bwd_common(const void* q, const void* k, const void* v, const v
   if (!ensure_init()) return FA_ERR_LAUNCH;
   const int tb = cu ? 1 : nbatch;
   CUtensorMap tq, tk, tv, tdo;
-  if (!make_tmap_bhnd(&tq, q, d, n_rows, H, tb) || !make_tmap_bhnd(&tk, k, d, n_rows, H, tb) ||
-      !make_tmap_bhnd(&tv, v, d, n_rows, H, tb) || !make_tmap_bhnd(&tdo, dout, d, n_rows, H, tb))
+  const int q_box = d == 128 ? 64 : 128;  // the d = 128 backward steps through 64 queries at a time
+  if (!make_tmap_bhnd(&tq, q, d, n_rows, H, tb, q_box) || !make_tmap_bhnd(&tk, k, d, n_rows, H, tb) ||
+      !make_tmap_bhnd(&tv, v, d, n_rows, H, tb) || !make_tmap_bhnd(&tdo, dout, d, n_rows, H, tb, q_box))
     return FA_ERR_INVALID_ARG;
   const size_t acc_bytes = align256((size_t)tb * n_rows * H * d * sizeof(float));
   const size_t row_bytes = align256((size_t)tb * H * n_rows * sizeof(float));

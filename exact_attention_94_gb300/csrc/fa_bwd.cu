@@ -55,6 +55,17 @@ struct BwdLayout {
 
 // ---------------------------------------------------------------- pre / post
 
+// The fp32 dQ accumulator is kept in one of two layouts (as float4 groups):
+//   d = 64 : [B*H][d/4][rows][4]  (the query-row threads of a warp add 512 contiguous bytes)
+//   d = 128: [B*H][rows][d]       (the d-row threads of a warp add 128 contiguous bytes)
+template <int D>
+__host__ __device__ __forceinline__ size_t acc_f4_index(size_t bh, int n_rows, int row, int c4) {
+  if constexpr (D == 128)
+    return (bh * n_rows + row) * (D / 4) + c4;
+  else
+    return (bh * (D / 4) + c4) * n_rows + row;
+}
+
 // One warp per row (b, h, n): D = sum_c dO * O, lse2 = lse * log2 e; the
 // dQ accumulator rows it owns are zeroed.  Tensors [Bt][rows][H][d].
 template <int D>
@@ -101,7 +112,7 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16* __
   }
   // zero this row of the accumulator: d/4 groups of 4 floats
   if (lane < D / 4) {
-    float4* dst = reinterpret_cast<float4*>(dq_acc) + ((size_t)bh * (D / 4) + lane) * n_rows + n;
+    float4* dst = reinterpret_cast<float4*>(dq_acc) + acc_f4_index<D>((size_t)bh, n_rows, n, lane);
     *dst = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
@@ -122,7 +133,7 @@ __global__ void __launch_bounds__(256) fa_bwd_post_kernel(const float* __restric
   const int n = (int)(r % n_rows);
   const long long bt = r / n_rows;
   const long long bh = bt * H + h;
-  const float4 v = reinterpret_cast<const float4*>(dq_acc)[((size_t)bh * G + c4) * n_rows + n];
+  const float4 v = reinterpret_cast<const float4*>(dq_acc)[acc_f4_index<D>((size_t)bh, n_rows, n, c4)];
   uint2 out;
   out.x = pack_bf16x2(v.x, v.y);
   out.y = pack_bf16x2(v.z, v.w);
@@ -309,17 +320,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int swz = kr & 7;
     uint8_t* ds_row = sbase + L::kDS + kr * 128;
     bool ok = true;
+    // this thread's lse2 and D of the next query block, fetched one step ahead
+    // (invalid rows: lse2 = +inf, so P = 0)
+    auto fetch = [&](int n, float& l2, float& ds) {
+      const int qg = (i_begin + n) * 128 + kr;
+      const bool qv = n < n_steps && qg < seq_len;
+      l2 = qv ? p.lse2[row_base + qg] : INFINITY;
+      ds = qv ? p.dsum[row_base + qg] : 0.f;
+    };
+    float pf_l, pf_d;
+    fetch(0, pf_l, pf_d);
     for (int n = 0; n < n_steps; ++n) {
       const int q0 = (i_begin + n) * 128;
-      // stage this query block's lse2 and D (invalid rows: lse2 = +inf, so P = 0)
       asm volatile("bar.sync 1, 128;" ::: "memory");
-      {
-        const int qg = q0 + kr;
-        const bool qv = qg < seq_len;
-        s_lse2[kr] = qv ? p.lse2[row_base + qg] : INFINITY;
-        s_dsum[kr] = qv ? p.dsum[row_base + qg] : 0.f;
-      }
+      s_lse2[kr] = pf_l;
+      s_dsum[kr] = pf_d;
       asm volatile("bar.sync 1, 128;" ::: "memory");
+      fetch(n + 1, pf_l, pf_d);
       // After an abort the warp keeps taking part in the two named barriers of every
       // step (so the other warps of the group never wait on it) and does nothing else.
       if (!ok) continue;
@@ -443,6 +460,378 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------- main, d = 128, pipelined
+//
+// Steps of 64 queries.  S^T and dP^T are double-buffered in TMEM, so while
+// warps 4-7 recompute P and dS for step n+1, the tensor pipe runs the
+// gradient products of step n and the two score products of step n+2.
+// dQ is produced transposed, dQ^T = K^T dS^T (M = d = 128 TMEM lanes), into
+// the S^T buffer of its step once dV has consumed that buffer's P^T.
+//   TMEM: S^T/P^T/dQ^T [0,64) and [64,128), dP^T [128,192) and [192,256),
+//         dV [256,384), dK [384,512).
+//   Shared: K_j, V_j 32 KB each; three stages of Q_i, dO_i (16 KB each);
+//           two dS^T buffers (128 keys x 64 queries, 16 KB each).
+constexpr int kBwd128Threads = 512;  // + a second recompute warpgroup
+
+struct Bwd128Layout {
+  static constexpr uint32_t kTileKV = 128u * 128u * 2u;  // 128 rows x 128 d
+  static constexpr uint32_t kChunkKV = 128u * 128u;      // 128 rows x 64 d
+  static constexpr uint32_t kTileQ = 64u * 128u * 2u;    // 64 rows x 128 d
+  static constexpr uint32_t kChunkQ = 64u * 128u;        // 64 rows x 64 d
+  static constexpr int kStages = 3;
+  static constexpr uint32_t kK = 0;
+  static constexpr uint32_t kV = kTileKV;
+  static constexpr uint32_t kStage0 = 2 * kTileKV;
+  static constexpr uint32_t kStageBytes = 2 * kTileQ;    // Q_i then dO_i
+  static constexpr uint32_t kDS0 = kStage0 + kStages * kStageBytes;
+  static constexpr uint32_t kDSBytes = 128u * 64u * 2u;
+  static constexpr uint32_t kBar = kDS0 + 2 * kDSBytes;
+  static constexpr uint32_t kBytes = kBar + 256 + 512 + 1024;  // barriers, lse2/D rows, alignment slack
+};
+
+template <bool CAUSAL>
+__global__ void __launch_bounds__(kBwd128Threads, 1)
+    fa_bwd_main128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                          const BwdParams p) {
+  using L = Bwd128Layout;
+  constexpr int D = 128;
+  constexpr int NST = L::kStages;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sbase = smem_raw + (base - raw);
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+
+  const int bh = (int)(blockIdx.z * gridDim.x + blockIdx.x);
+  if (bh >= p.B * p.H) return;
+  const int b = bh / p.H;
+  const int h = bh % p.H;
+  const int jb = (int)blockIdx.y;
+  int seq_start = 0, seq_len = p.seq_len, b_coord = b;
+  if (p.cu_seqlens != nullptr) {
+    seq_start = p.cu_seqlens[b];
+    seq_len = p.cu_seqlens[b + 1] - seq_start;
+    b_coord = 0;
+  }
+  const int k0 = jb * 128;
+  if (k0 >= seq_len) return;
+  const int q_begin = CAUSAL ? k0 : 0;                 // first query of the first step
+  const int n_steps = (seq_len - q_begin + 63) / 64;   // 64 queries per step
+  const size_t row_base = (size_t)(b_coord * p.H + h) * p.n_rows + seq_start;
+
+  enum { KV_FULL = 0, Q_FULL = 1, STAGE_EMPTY = Q_FULL + NST, SD_FULL = STAGE_EMPTY + NST, P_READY = SD_FULL + 2,
+         DQ_FULL = P_READY + 2, DQ_EMPTY = DQ_FULL + 2, DKV_FINAL = DQ_EMPTY + 2, DRAIN, NBARS };
+  const uint32_t bar0 = base + L::kBar;
+  auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + L::kBar + 8 * NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* s_lse2 = reinterpret_cast<float*>(sbase + L::kBar + 256);  // 64 floats
+  float* s_dsum = s_lse2 + 64;                                      // 64 floats
+
+  if (threadIdx.x == 0) {
+    mbar_init(BAR(KV_FULL), 1);
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(BAR(Q_FULL + s), 1);
+      mbar_init(BAR(STAGE_EMPTY + s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(BAR(SD_FULL + i), 1);
+      mbar_init(BAR(P_READY + i), 256);
+      mbar_init(BAR(DQ_FULL + i), 1);
+      mbar_init(BAR(DQ_EMPTY + i), 128);
+    }
+    mbar_init(BAR(DKV_FINAL), 1);
+    mbar_init(BAR(DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtx w{abort_flag, p.timeout_ns, p.err};
+
+  const uint32_t sK = base + L::kK, sV = base + L::kV;
+  auto stage_q = [&](int st) -> uint32_t { return base + L::kStage0 + (uint32_t)st * L::kStageBytes; };
+  auto sds = [&](int i) -> uint32_t { return base + L::kDS0 + (uint32_t)i * L::kDSBytes; };
+
+  if (warp == 0) {
+    // ============================================================ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      mbar_arrive_expect_tx(BAR(KV_FULL), 2 * L::kTileKV);
+      for (int c = 0; c < 2; ++c) {
+        tma_load_4d(sK + c * L::kChunkKV, &tm_k, BAR(KV_FULL), c * 64, seq_start + k0, h, b_coord);
+        tma_load_4d(sV + c * L::kChunkKV, &tm_v, BAR(KV_FULL), c * 64, seq_start + k0, h, b_coord);
+      }
+      bool ok = true;
+      for (int n = 0; n < n_steps && ok; ++n) {
+        const int st = n % NST;
+        const int row = seq_start + q_begin + n * 64;
+        if (n >= NST && !(ok = mbar_wait(BAR(STAGE_EMPTY + st), ((n / NST) - 1) & 1, w, 51))) break;
+        mbar_arrive_expect_tx(BAR(Q_FULL + st), 2 * L::kTileQ);
+        const uint32_t qa = stage_q(st);
+        for (int c = 0; c < 2; ++c) {
+          tma_load_4d(qa + c * L::kChunkQ, &tm_q, BAR(Q_FULL + st), c * 64, row, h, b_coord);
+          tma_load_4d(qa + L::kTileQ + c * L::kChunkQ, &tm_do, BAR(Q_FULL + st), c * 64, row, h, b_coord);
+        }
+      }
+      if (!ok) {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 200000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ============================================================ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_SD = idesc_bf16(128, 64, false, false);  // S^T, dP^T: M keys, N queries
+      constexpr uint32_t IDESC_KV = idesc_bf16(128, 128, false, true);  // dV, dK: M keys, N d
+      constexpr uint32_t IDESC_DQ = idesc_bf16(128, 64, true, true);    // dQ^T: M d, N queries
+      const uint32_t tDV = tmem + 256, tDK = tmem + 384;
+      auto tS = [&](int i) -> uint32_t { return tmem + 64u * (uint32_t)i; };
+      auto tDP = [&](int i) -> uint32_t { return tmem + 128u + 64u * (uint32_t)i; };
+      // Base descriptors built once; each product below only advances the start
+      // address by a compile-time offset, so one thread keeps the tensor pipe fed.
+      const uint64_t dK_kmaj = smem_desc_sw128(sK, 16, 1024);          // K_j as K-major A (S^T)
+      const uint64_t dV_kmaj = smem_desc_sw128(sV, 16, 1024);          // V_j as K-major A (dP^T)
+      const uint64_t dK_mn = smem_desc_sw128(sK, L::kChunkKV, 1024);   // K_j^T as MN-major A (dQ^T)
+      const uint64_t dDS_k[2] = {smem_desc_sw128(sds(0), 16, 1024), smem_desc_sw128(sds(1), 16, 1024)};
+      const uint64_t dDS_mn[2] = {smem_desc_sw128(sds(0), L::kChunkQ, 1024),
+                                  smem_desc_sw128(sds(1), L::kChunkQ, 1024)};
+      // dP^T(n) = V_j dO_n^T and S^T(n) = K_j Q_n^T (both operands K-major)
+      auto issue_dp = [&](int n) {
+        const uint64_t db = smem_desc_sw128(stage_q(n % NST) + L::kTileQ, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tDP(n & 1), desc_add(dV_kmaj, (kk / 4) * L::kChunkKV + (kk % 4) * 32),
+                 desc_add(db, (kk / 4) * L::kChunkQ + (kk % 4) * 32), IDESC_SD, kk > 0);
+      };
+      auto issue_s = [&](int n) {
+        const uint64_t qb = smem_desc_sw128(stage_q(n % NST), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tS(n & 1), desc_add(dK_kmaj, (kk / 4) * L::kChunkKV + (kk % 4) * 32),
+                 desc_add(qb, (kk / 4) * L::kChunkQ + (kk % 4) * 32), IDESC_SD, kk > 0);
+      };
+      bool ok = mbar_wait(BAR(KV_FULL), 0, w, 52);
+      tc_fence_after();
+      for (int n = 0; n < 2 && n < n_steps && ok; ++n) {
+        if (!(ok = mbar_wait(BAR(Q_FULL + n), 0, w, 53))) break;
+        tc_fence_after();
+        issue_s(n);
+        issue_dp(n);
+        mma_commit(BAR(SD_FULL + n));
+      }
+      for (int n = 0; n < n_steps && ok; ++n) {
+        const int bb = n & 1, st = n % NST;
+        const uint32_t qa = stage_q(st), da = qa + L::kTileQ;
+        if (!(ok = mbar_wait(BAR(P_READY + bb), (n >> 1) & 1, w, 54))) break;
+        tc_fence_after();
+        const uint64_t q_mn = smem_desc_sw128(qa, L::kChunkQ, 1024), do_mn = smem_desc_sw128(da, L::kChunkQ, 1024);
+        // dV += P^T dO_n  (A = P^T from TMEM; B = dO_n MN-major; K = 64 queries)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ts(tDV, tS(bb) + (kk >> 1) * 32 + (kk & 1) * 8, desc_add(do_mn, kk * 2048), IDESC_KV,
+                 (n > 0 || kk > 0) ? 1u : 0u);
+        // dK += dS^T Q_n  (A = dS^T K-major; B = Q_n MN-major)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ss(tDK, desc_add(dDS_k[bb], kk * 32), desc_add(q_mn, kk * 2048), IDESC_KV, (n > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(BAR(STAGE_EMPTY + st));
+        // dQ^T = K_j^T dS^T  (A = K_j MN-major over d; B = dS^T MN-major over queries; K = 128 keys),
+        // into this step's S^T columns, whose P^T the dV product above has consumed
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tS(bb), desc_add(dK_mn, kk * 2048), desc_add(dDS_mn[bb], kk * 2048), IDESC_DQ, kk > 0);
+        mma_commit(BAR(DQ_FULL + bb));
+        if (n + 2 < n_steps) {
+          if (!(ok = mbar_wait(BAR(Q_FULL + (n + 2) % NST), ((n + 2) / NST) & 1, w, 55))) break;
+          tc_fence_after();
+          issue_dp(n + 2);  // step n's dP^T was read before P_READY
+          if (!(ok = mbar_wait(BAR(DQ_EMPTY + bb), (n >> 1) & 1, w, 56))) break;
+          tc_fence_after();
+          issue_s(n + 2);   // dQ^T of step n has left these columns
+          mma_commit(BAR(SD_FULL + bb));
+        }
+      }
+      if (ok) mma_commit(BAR(DKV_FINAL));
+      mma_commit(BAR(DRAIN));
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(BAR(DRAIN), 0) && globaltimer_ns() - t0 < p.timeout_ns) {
+      }
+    }
+  } else if (warp >= 4 && warp < 12) {
+    // ============================================================ P and dS (thread = key row)
+    // Two warpgroups: group g owns the step's queries [32g, 32g+32).  P^T for
+    // query q goes to TMEM column 32*(q/32) + (q%32)/2, i.e. over the group's own
+    // already-read S^T columns, so the groups never touch each other's scores.
+    const int g = (warp - 4) >> 2;
+    const int kw = warp & 3;
+    const int kr = kw * 32 + lane;
+    const int kg = k0 + kr;
+    const bool row_ok = kg < seq_len;
+    const uint32_t lane_off = (uint32_t)(kw * 32) << 16;
+    const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
+    const uint64_t scale2 = f2_pack(p.scale, p.scale);
+    const int swz = kr & 7;
+    float* my_lse2 = s_lse2 + 32 * g;
+    float* my_dsum = s_dsum + 32 * g;
+    // Threads 0-31 of the group carry one lse2 value, threads 32-63 one D value,
+    // fetched from global memory one step ahead so the load latency never sits
+    // on a step's critical path.  Queries past the end: lse2 = +inf (P = 0), D = 0.
+    auto fetch = [&](int n) -> float {
+      const int qg = q_begin + n * 64 + 32 * g + (kr & 31);
+      if (kr >= 64 || n >= n_steps) return 0.f;
+      if (qg >= seq_len) return kr < 32 ? INFINITY : 0.f;
+      return kr < 32 ? p.lse2[row_base + qg] : p.dsum[row_base + qg];
+    };
+    float pf = fetch(0);
+    bool ok = true;
+    for (int n = 0; n < n_steps; ++n) {
+      const int bb = n & 1;
+      const int q0 = q_begin + n * 64 + 32 * g;  // first query of this group's slice
+      asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory");
+      if (kr < 32)
+        my_lse2[kr] = pf;
+      else if (kr < 64)
+        my_dsum[kr - 32] = pf;
+      asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory");
+      pf = fetch(n + 1);
+      // After an abort the warp keeps taking part in the named barriers and does nothing else.
+      if (!ok) continue;
+      ok = mbar_wait(BAR(SD_FULL + bb), (n >> 1) & 1, w, 57) &&
+           (n < 2 || mbar_wait(BAR(DQ_FULL + bb), ((n - 2) >> 1) & 1, w, 58));  // dS^T buffer free
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        continue;
+      }
+      tc_fence_after();
+      const bool diag = CAUSAL && (q0 < k0 + 127);
+      const uint32_t tSb = tmem + lane_off + 64u * bb + 32u * g;
+      const uint32_t tDPb = tmem + lane_off + 128u + 64u * bb + 32u * g;
+      uint32_t sr[32], dr[32];
+      tmem_ld16(tSb, sr);
+      tmem_ld16(tSb + 16, sr + 16);
+      tmem_ld16(tDPb, dr);
+      tmem_ld16(tDPb + 16, dr + 16);
+      tmem_ld_wait();
+      uint32_t pp[16], dd[16];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const float4* l4 = reinterpret_cast<const float4*>(my_lse2 + 16 * c);
+        const float4* d4 = reinterpret_cast<const float4*>(my_dsum + 16 * c);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const float4 lv = l4[q4], dv = d4[q4];
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int e = 16 * c + 4 * q4 + 2 * h2;  // element pair (e, e+1) of the slice
+            const float la = h2 ? lv.z : lv.x, lb = h2 ? lv.w : lv.y;
+            const float da = h2 ? dv.z : dv.x, db = h2 ? dv.w : dv.y;
+            float y0, y1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl2x2, f2_pack(-la, -lb)),
+                      y0, y1);
+            float p0 = ex2_sfu(y0), p1 = ex2_sfu(y1);
+            if (!row_ok) {
+              p0 = 0.f;
+              p1 = 0.f;
+            }
+            if (diag) {
+              const int qg = q0 + e;
+              if (kg > qg) p0 = 0.f;
+              if (kg > qg + 1) p1 = 0.f;
+            }
+            const uint64_t pv = f2_pack(p0, p1);
+            const uint64_t t = f2_add(f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), f2_pack(-da, -db));
+            float g0, g1;
+            f2_unpack(f2_mul(f2_mul(pv, scale2), t), g0, g1);
+            pp[e / 2] = pack_bf16x2(p0, p1);
+            dd[e / 2] = pack_bf16x2(g0, g1);
+          }
+        }
+      }
+      tmem_st8(tSb, pp);  // queries 32g .. 32g+15
+      tmem_st8(tSb + 8, pp + 8);
+      uint8_t* ds_row = sbase + L::kDS0 + bb * L::kDSBytes + kr * 128;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        *reinterpret_cast<uint4*>(ds_row + (((4 * g + u) ^ swz) << 4)) =
+            make_uint4(dd[4 * u], dd[4 * u + 1], dd[4 * u + 2], dd[4 * u + 3]);
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(BAR(P_READY + bb));
+    }
+    // ------------------------------------------------------------ epilogue: group 0 writes dV, group 1 dK
+    if (ok) {
+      ok = mbar_wait(BAR(DKV_FINAL), 0, w, 59);
+      if (__all_sync(0xffffffffu, ok)) {
+        tc_fence_after();
+        const size_t grow = ((size_t)b_coord * p.n_rows + seq_start + kg) * p.H + h;
+        const uint32_t src = tmem + lane_off + (g ? 384u : 256u);
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(g ? p.dk : p.dv) + grow * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(src + 32 * c, v);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+          if (row_ok) {
+            uint4* o4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+      }
+    }
+  } else if (warp >= 12) {
+    // ============================================================ dQ drain (thread = one of the d rows of dQ^T)
+    const int qw = warp & 3;
+    const int dr = qw * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
+    float* acc = p.dq_acc + row_base * D + dr;  // [B*H][rows][d]: a warp's lanes cover 128 contiguous bytes
+    for (int n = 0; n < n_steps; ++n) {
+      const int bb = n & 1;
+      const int q0 = q_begin + n * 64;
+      bool ok = mbar_wait(BAR(DQ_FULL + bb), (n >> 1) & 1, w, 60);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      uint32_t v[64];
+      tmem_ld32(tmem + lane_off + 64u * bb, *reinterpret_cast<uint32_t(*)[32]>(v));
+      tmem_ld32(tmem + lane_off + 64u * bb + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(BAR(DQ_EMPTY + bb));  // the columns are free for S^T of step n+2
+      const int nq = min(64, seq_len - q0);
+#pragma unroll
+      for (int j = 0; j < 64; ++j)
+        if (j < nq) atomicAdd(acc + (size_t)(q0 + j) * D, __uint_as_float(v[j]));
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 template <int D, bool CAUSAL>
 static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream) {
@@ -453,8 +842,8 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
-  auto kern = fa_bwd_main_kernel<D, CAUSAL>;
-  constexpr uint32_t smem = BwdLayout<D>::kBytes;
+  auto kern = D == 128 ? fa_bwd_main128_kernel<CAUSAL> : fa_bwd_main_kernel<D, CAUSAL>;
+  constexpr uint32_t smem = D == 128 ? Bwd128Layout::kBytes : BwdLayout<D>::kBytes;
   static bool configured = false;
   if (!configured) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -464,7 +853,7 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
   const int bh = p.B * p.H;
   const int gx = bh < kBwdHeadGroup ? bh : kBwdHeadGroup;
   dim3 grid(gx, p.num_kblocks, (bh + gx - 1) / gx);
-  kern<<<grid, kBwdThreads, smem, stream>>>(tq, tk, tv, tdo, p);
+  kern<<<grid, D == 128 ? kBwd128Threads : kBwdThreads, smem, stream>>>(tq, tk, tv, tdo, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 

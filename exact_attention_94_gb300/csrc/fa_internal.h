@@ -47,9 +47,9 @@ struct BwdParams {
   unsigned long long timeout_ns;
 };
 
-// Encodes a 4-D bf16 tensor map over [B][n_rows][H][D] with a 128-row x 64-column
+// Encodes a 4-D bf16 tensor map over [B][n_rows][H][D] with a box_rows x 64-column
 // box and 128-byte swizzle.  Returns false when the driver refuses it.
-bool make_tmap_bhnd(CUtensorMap* m, const void* ptr, int D, int n_rows, int H, int B);
+bool make_tmap_bhnd(CUtensorMap* m, const void* ptr, int D, int n_rows, int H, int B, int box_rows = 128);
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                        int D, bool causal, bool poly, int grid_x, cudaStream_t stream);

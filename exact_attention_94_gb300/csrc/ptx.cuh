@@ -164,6 +164,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// Advances a descriptor's start address by a byte offset (a multiple of 16).
+// Shared-memory addresses stay below 2^18 bytes, so the 14-bit address field
+// never carries into the neighbouring fields.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t byte_off) {
+  return desc + (uint64_t)(byte_off >> 4);
+}
+
 // Instruction descriptor for kind::f16 with bf16 inputs and fp32 accumulation.
 // a_mn / b_mn: operand stored MN-major (transposed) instead of K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
