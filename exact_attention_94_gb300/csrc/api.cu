@@ -197,7 +197,7 @@ static fa_status bwd_common(const void* q, const void* k, const void* v, const v
   if (!ensure_init()) return FA_ERR_LAUNCH;
   const int tb = cu ? 1 : nbatch;
   CUtensorMap tq, tk, tv, tdo;
-  const int q_box = d == 128 ? 64 : 128;  // the d = 128 backward steps through 64 queries at a time
+  const int q_box = 128;
   if (!make_tmap_bhnd(&tq, q, d, n_rows, H, tb, q_box) || !make_tmap_bhnd(&tk, k, d, n_rows, H, tb) ||
       !make_tmap_bhnd(&tv, v, d, n_rows, H, tb) || !make_tmap_bhnd(&tdo, dout, d, n_rows, H, tb, q_box))
     return FA_ERR_INVALID_ARG;

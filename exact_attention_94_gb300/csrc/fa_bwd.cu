@@ -460,33 +460,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-// ---------------------------------------------------------------- main, d = 128, pipelined
+// ---------------------------------------------------------------- main, d = 128, overlapped
 //
-// Steps of 64 queries.  S^T and dP^T are double-buffered in TMEM, so while
-// warps 4-7 recompute P and dS for step n+1, the tensor pipe runs the
-// gradient products of step n and the two score products of step n+2.
-// dQ is produced transposed, dQ^T = K^T dS^T (M = d = 128 TMEM lanes), into
-// the S^T buffer of its step once dV has consumed that buffer's P^T.
-//   TMEM: S^T/P^T/dQ^T [0,64) and [64,128), dP^T [128,192) and [192,256),
-//         dV [256,384), dK [384,512).
-//   Shared: K_j, V_j 32 KB each; three stages of Q_i, dO_i (16 KB each);
-//           two dS^T buffers (128 keys x 64 queries, 16 KB each).
-constexpr int kBwd128Threads = 512;  // + a second recompute warpgroup
+// Steps of 128 queries, so every product is an M = 128, N = 128 tcgen05.mma
+// (a measured 8192 FLOP/clk/SM; N = 64 reaches only two thirds of that).
+// Two warpgroups recompute P and dS: group g owns the step's queries
+// [64g, 64g+64) and hands them to the tensor pipe in two quarters of 32, so
+// dV and dK of one quarter run while the next quarter is being recomputed.
+// dQ is produced transposed, dQ^T = K^T dS^T (M = d), into the dP^T columns
+// once both groups have read them, and drained while S^T of the next step runs.
+//   TMEM: S^T/P^T [0,128), dP^T/dQ^T [128,256), dV [256,384), dK [384,512).
+//   P^T of query q sits at column 64*(q/64) + (q%64)/2: over the recomputing
+//   group's own, already-read S^T columns.
+//   Shared: K_j, V_j 32 KB each; two stages of Q_i, dO_i (32 KB each);
+//           dS^T 128 keys x 128 queries (two 64-query chunks).
+constexpr int kBwd128Threads = 512;
 
 struct Bwd128Layout {
-  static constexpr uint32_t kTileKV = 128u * 128u * 2u;  // 128 rows x 128 d
-  static constexpr uint32_t kChunkKV = 128u * 128u;      // 128 rows x 64 d
-  static constexpr uint32_t kTileQ = 64u * 128u * 2u;    // 64 rows x 128 d
-  static constexpr uint32_t kChunkQ = 64u * 128u;        // 64 rows x 64 d
-  static constexpr int kStages = 3;
+  static constexpr uint32_t kTile = 128u * 128u * 2u;  // 128 rows x 128 d
+  static constexpr uint32_t kChunk = 128u * 128u;      // 128 rows x 64 columns
+  static constexpr int kStages = 2;
   static constexpr uint32_t kK = 0;
-  static constexpr uint32_t kV = kTileKV;
-  static constexpr uint32_t kStage0 = 2 * kTileKV;
-  static constexpr uint32_t kStageBytes = 2 * kTileQ;    // Q_i then dO_i
-  static constexpr uint32_t kDS0 = kStage0 + kStages * kStageBytes;
-  static constexpr uint32_t kDSBytes = 128u * 64u * 2u;
-  static constexpr uint32_t kBar = kDS0 + 2 * kDSBytes;
-  static constexpr uint32_t kBytes = kBar + 256 + 512 + 1024;  // barriers, lse2/D rows, alignment slack
+  static constexpr uint32_t kV = kTile;
+  static constexpr uint32_t kStage0 = 2 * kTile;
+  static constexpr uint32_t kStageBytes = 2 * kTile;  // Q_i then dO_i
+  static constexpr uint32_t kDS = kStage0 + kStages * kStageBytes;
+  static constexpr uint32_t kBar = kDS + 2 * kChunk;
+  static constexpr uint32_t kBytes = kBar + 256 + 1024 + 1024;  // barriers, lse2/D rows, alignment slack
 };
 
 template <bool CAUSAL>
@@ -497,6 +497,7 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
   using L = Bwd128Layout;
   constexpr int D = 128;
   constexpr int NST = L::kStages;
+  constexpr uint32_t CHUNK = L::kChunk;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -519,18 +520,19 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
   }
   const int k0 = jb * 128;
   if (k0 >= seq_len) return;
-  const int q_begin = CAUSAL ? k0 : 0;                 // first query of the first step
-  const int n_steps = (seq_len - q_begin + 63) / 64;   // 64 queries per step
+  const int q_begin = CAUSAL ? k0 : 0;
+  const int n_steps = (seq_len - q_begin + 127) / 128;
   const size_t row_base = (size_t)(b_coord * p.H + h) * p.n_rows + seq_start;
 
-  enum { KV_FULL = 0, Q_FULL = 1, STAGE_EMPTY = Q_FULL + NST, SD_FULL = STAGE_EMPTY + NST, P_READY = SD_FULL + 2,
-         DQ_FULL = P_READY + 2, DQ_EMPTY = DQ_FULL + 2, DKV_FINAL = DQ_EMPTY + 2, DRAIN, NBARS };
+  enum { KV_FULL = 0, Q_FULL = 1, STAGE_EMPTY = Q_FULL + NST, S_FULL = STAGE_EMPTY + NST, DP_FULL = S_FULL + 1,
+         P_READY = DP_FULL + 1,
+         DQ_FULL = P_READY + 4, DQ_EMPTY, DKV_FINAL, DRAIN, NBARS };
   const uint32_t bar0 = base + L::kBar;
   auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + L::kBar + 8 * NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* s_lse2 = reinterpret_cast<float*>(sbase + L::kBar + 256);  // 64 floats
-  float* s_dsum = s_lse2 + 64;                                      // 64 floats
+  float* s_lse2 = reinterpret_cast<float*>(sbase + L::kBar + 256);  // 128 floats
+  float* s_dsum = s_lse2 + 128;                                     // 128 floats
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(KV_FULL), 1);
@@ -538,12 +540,11 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
       mbar_init(BAR(Q_FULL + s), 1);
       mbar_init(BAR(STAGE_EMPTY + s), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(BAR(SD_FULL + i), 1);
-      mbar_init(BAR(P_READY + i), 256);
-      mbar_init(BAR(DQ_FULL + i), 1);
-      mbar_init(BAR(DQ_EMPTY + i), 128);
-    }
+    mbar_init(BAR(S_FULL), 1);
+    mbar_init(BAR(DP_FULL), 1);
+    for (int i = 0; i < 4; ++i) mbar_init(BAR(P_READY + i), 128);
+    mbar_init(BAR(DQ_FULL), 1);
+    mbar_init(BAR(DQ_EMPTY), 128);
     mbar_init(BAR(DKV_FINAL), 1);
     mbar_init(BAR(DRAIN), 1);
     *abort_flag = 0;
@@ -559,9 +560,8 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtx w{abort_flag, p.timeout_ns, p.err};
 
-  const uint32_t sK = base + L::kK, sV = base + L::kV;
+  const uint32_t sK = base + L::kK, sV = base + L::kV, sDS = base + L::kDS;
   auto stage_q = [&](int st) -> uint32_t { return base + L::kStage0 + (uint32_t)st * L::kStageBytes; };
-  auto sds = [&](int i) -> uint32_t { return base + L::kDS0 + (uint32_t)i * L::kDSBytes; };
 
   if (warp == 0) {
     // ============================================================ TMA producer
@@ -570,21 +570,21 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
-      mbar_arrive_expect_tx(BAR(KV_FULL), 2 * L::kTileKV);
+      mbar_arrive_expect_tx(BAR(KV_FULL), 2 * L::kTile);
       for (int c = 0; c < 2; ++c) {
-        tma_load_4d(sK + c * L::kChunkKV, &tm_k, BAR(KV_FULL), c * 64, seq_start + k0, h, b_coord);
-        tma_load_4d(sV + c * L::kChunkKV, &tm_v, BAR(KV_FULL), c * 64, seq_start + k0, h, b_coord);
+        tma_load_4d(sK + c * CHUNK, &tm_k, BAR(KV_FULL), c * 64, seq_start + k0, h, b_coord);
+        tma_load_4d(sV + c * CHUNK, &tm_v, BAR(KV_FULL), c * 64, seq_start + k0, h, b_coord);
       }
       bool ok = true;
       for (int n = 0; n < n_steps && ok; ++n) {
         const int st = n % NST;
-        const int row = seq_start + q_begin + n * 64;
+        const int row = seq_start + q_begin + n * 128;
         if (n >= NST && !(ok = mbar_wait(BAR(STAGE_EMPTY + st), ((n / NST) - 1) & 1, w, 51))) break;
-        mbar_arrive_expect_tx(BAR(Q_FULL + st), 2 * L::kTileQ);
+        mbar_arrive_expect_tx(BAR(Q_FULL + st), 2 * L::kTile);
         const uint32_t qa = stage_q(st);
         for (int c = 0; c < 2; ++c) {
-          tma_load_4d(qa + c * L::kChunkQ, &tm_q, BAR(Q_FULL + st), c * 64, row, h, b_coord);
-          tma_load_4d(qa + L::kTileQ + c * L::kChunkQ, &tm_do, BAR(Q_FULL + st), c * 64, row, h, b_coord);
+          tma_load_4d(qa + c * CHUNK, &tm_q, BAR(Q_FULL + st), c * 64, row, h, b_coord);
+          tma_load_4d(qa + L::kTile + c * CHUNK, &tm_do, BAR(Q_FULL + st), c * 64, row, h, b_coord);
         }
       }
       if (!ok) {
@@ -596,75 +596,66 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
   } else if (warp == 1) {
     // ============================================================ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t IDESC_SD = idesc_bf16(128, 64, false, false);  // S^T, dP^T: M keys, N queries
-      constexpr uint32_t IDESC_KV = idesc_bf16(128, 128, false, true);  // dV, dK: M keys, N d
-      constexpr uint32_t IDESC_DQ = idesc_bf16(128, 64, true, true);    // dQ^T: M d, N queries
-      const uint32_t tDV = tmem + 256, tDK = tmem + 384;
-      auto tS = [&](int i) -> uint32_t { return tmem + 64u * (uint32_t)i; };
-      auto tDP = [&](int i) -> uint32_t { return tmem + 128u + 64u * (uint32_t)i; };
-      // Base descriptors built once; each product below only advances the start
-      // address by a compile-time offset, so one thread keeps the tensor pipe fed.
-      const uint64_t dK_kmaj = smem_desc_sw128(sK, 16, 1024);          // K_j as K-major A (S^T)
-      const uint64_t dV_kmaj = smem_desc_sw128(sV, 16, 1024);          // V_j as K-major A (dP^T)
-      const uint64_t dK_mn = smem_desc_sw128(sK, L::kChunkKV, 1024);   // K_j^T as MN-major A (dQ^T)
-      const uint64_t dDS_k[2] = {smem_desc_sw128(sds(0), 16, 1024), smem_desc_sw128(sds(1), 16, 1024)};
-      const uint64_t dDS_mn[2] = {smem_desc_sw128(sds(0), L::kChunkQ, 1024),
-                                  smem_desc_sw128(sds(1), L::kChunkQ, 1024)};
-      // dP^T(n) = V_j dO_n^T and S^T(n) = K_j Q_n^T (both operands K-major)
-      auto issue_dp = [&](int n) {
-        const uint64_t db = smem_desc_sw128(stage_q(n % NST) + L::kTileQ, 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tDP(n & 1), desc_add(dV_kmaj, (kk / 4) * L::kChunkKV + (kk % 4) * 32),
-                 desc_add(db, (kk / 4) * L::kChunkQ + (kk % 4) * 32), IDESC_SD, kk > 0);
-      };
-      auto issue_s = [&](int n) {
-        const uint64_t qb = smem_desc_sw128(stage_q(n % NST), 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tS(n & 1), desc_add(dK_kmaj, (kk / 4) * L::kChunkKV + (kk % 4) * 32),
-                 desc_add(qb, (kk / 4) * L::kChunkQ + (kk % 4) * 32), IDESC_SD, kk > 0);
-      };
+      constexpr uint32_t IDESC_SD = idesc_bf16(128, 128, false, false);  // S^T, dP^T: M keys, N queries
+      constexpr uint32_t IDESC_KV = idesc_bf16(128, 128, false, true);   // dV, dK: M keys, N d
+      constexpr uint32_t IDESC_DQ = idesc_bf16(128, 128, true, true);    // dQ^T: M d, N queries
+      const uint32_t tS = tmem, tDP = tmem + 128, tDV = tmem + 256, tDK = tmem + 384;
+      // base descriptors; each product only advances the start address
+      const uint64_t dK_kmaj = smem_desc_sw128(sK, 16, 1024);
+      const uint64_t dV_kmaj = smem_desc_sw128(sV, 16, 1024);
+      const uint64_t dK_mn = smem_desc_sw128(sK, CHUNK, 1024);   // K_j^T as MN-major A over d
+      const uint64_t dDS_k = smem_desc_sw128(sDS, 16, 1024);     // dS^T as K-major A (rows = keys)
+      const uint64_t dDS_mn = smem_desc_sw128(sDS, CHUNK, 1024); // dS^T as MN-major B over queries
       bool ok = mbar_wait(BAR(KV_FULL), 0, w, 52);
       tc_fence_after();
-      for (int n = 0; n < 2 && n < n_steps && ok; ++n) {
-        if (!(ok = mbar_wait(BAR(Q_FULL + n), 0, w, 53))) break;
-        tc_fence_after();
-        issue_s(n);
-        issue_dp(n);
-        mma_commit(BAR(SD_FULL + n));
-      }
       for (int n = 0; n < n_steps && ok; ++n) {
-        const int bb = n & 1, st = n % NST;
-        const uint32_t qa = stage_q(st), da = qa + L::kTileQ;
-        if (!(ok = mbar_wait(BAR(P_READY + bb), (n >> 1) & 1, w, 54))) break;
+        const int st = n % NST;
+        const uint32_t qa = stage_q(st), da = qa + L::kTile;
+        if (!(ok = mbar_wait(BAR(Q_FULL + st), (n / NST) & 1, w, 53))) break;
         tc_fence_after();
-        const uint64_t q_mn = smem_desc_sw128(qa, L::kChunkQ, 1024), do_mn = smem_desc_sw128(da, L::kChunkQ, 1024);
-        // dV += P^T dO_n  (A = P^T from TMEM; B = dO_n MN-major; K = 64 queries)
+        const uint64_t q_k = smem_desc_sw128(qa, 16, 1024), do_k = smem_desc_sw128(da, 16, 1024);
+        const uint64_t q_mn = smem_desc_sw128(qa, CHUNK, 1024), do_mn = smem_desc_sw128(da, CHUNK, 1024);
+        // S^T = K_j Q_i^T (the previous step's P^T was consumed by its dV products, issued earlier)
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ts(tDV, tS(bb) + (kk >> 1) * 32 + (kk & 1) * 8, desc_add(do_mn, kk * 2048), IDESC_KV,
-                 (n > 0 || kk > 0) ? 1u : 0u);
-        // dK += dS^T Q_n  (A = dS^T K-major; B = Q_n MN-major)
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk / 4) * CHUNK + (kk % 4) * 32;
+          mma_ss(tS, desc_add(dK_kmaj, off), desc_add(q_k, off), IDESC_SD, kk > 0);
+        }
+        mma_commit(BAR(S_FULL));  // P can be recomputed while dP^T is still running
+        if (n > 0) {  // the previous dQ^T must have left the dP^T columns
+          if (!(ok = mbar_wait(BAR(DQ_EMPTY), (n - 1) & 1, w, 54))) break;
+          tc_fence_after();
+        }
+        // dP^T = V_j dO_i^T
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ss(tDK, desc_add(dDS_k[bb], kk * 32), desc_add(q_mn, kk * 2048), IDESC_KV, (n > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk / 4) * CHUNK + (kk % 4) * 32;
+          mma_ss(tDP, desc_add(dV_kmaj, off), desc_add(do_k, off), IDESC_SD, kk > 0);
+        }
+        mma_commit(BAR(DP_FULL));
+        // dV += P^T dO_i and dK += dS^T Q_i, one 32-query quarter at a time as the groups hand them over:
+        // quarter i = group (i & 1), half (i >> 1); queries qb .. qb+31 with qb = 64*group + 32*half
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int g = i & 1, r = i >> 1;
+          const int qb = 64 * g + 32 * r;
+          if (!(ok = mbar_wait(BAR(P_READY + i), n & 1, w, 55))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {
+            const uint32_t acc = (n > 0 || i > 0 || kk > 0) ? 1u : 0u;
+            const uint32_t rows = (uint32_t)(qb / 16 + kk) * 2048;  // 16 query rows of Q_i / dO_i
+            mma_ts(tDV, tS + 64 * g + 16 * r + 8 * kk, desc_add(do_mn, rows), IDESC_KV, acc);
+            mma_ss(tDK, desc_add(dDS_k, g * CHUNK + (2 * r + kk) * 32), desc_add(q_mn, rows), IDESC_KV, acc);
+          }
+        }
+        if (!ok) break;
         mma_commit(BAR(STAGE_EMPTY + st));
-        // dQ^T = K_j^T dS^T  (A = K_j MN-major over d; B = dS^T MN-major over queries; K = 128 keys),
-        // into this step's S^T columns, whose P^T the dV product above has consumed
+        // dQ^T = K_j^T dS^T (M = d, N = 128 queries over both dS^T chunks, K = 128 keys) into the dP^T columns
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tS(bb), desc_add(dK_mn, kk * 2048), desc_add(dDS_mn[bb], kk * 2048), IDESC_DQ, kk > 0);
-        mma_commit(BAR(DQ_FULL + bb));
-        if (n + 2 < n_steps) {
-          if (!(ok = mbar_wait(BAR(Q_FULL + (n + 2) % NST), ((n + 2) / NST) & 1, w, 55))) break;
-          tc_fence_after();
-          issue_dp(n + 2);  // step n's dP^T was read before P_READY
-          if (!(ok = mbar_wait(BAR(DQ_EMPTY + bb), (n >> 1) & 1, w, 56))) break;
-          tc_fence_after();
-          issue_s(n + 2);   // dQ^T of step n has left these columns
-          mma_commit(BAR(SD_FULL + bb));
-        }
+          mma_ss(tDP, desc_add(dK_mn, kk * 2048), desc_add(dDS_mn, kk * 2048), IDESC_DQ, kk > 0);
+        mma_commit(BAR(DQ_FULL));
       }
       if (ok) mma_commit(BAR(DKV_FINAL));
       mma_commit(BAR(DRAIN));
@@ -674,10 +665,7 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
     }
   } else if (warp >= 4 && warp < 12) {
     // ============================================================ P and dS (thread = key row)
-    // Two warpgroups: group g owns the step's queries [32g, 32g+32).  P^T for
-    // query q goes to TMEM column 32*(q/32) + (q%32)/2, i.e. over the group's own
-    // already-read S^T columns, so the groups never touch each other's scores.
-    const int g = (warp - 4) >> 2;
+    const int g = (warp - 4) >> 2;  // group: queries [64g, 64g+64) of each step
     const int kw = warp & 3;
     const int kr = kw * 32 + lane;
     const int kg = k0 + kr;
@@ -686,58 +674,63 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
     const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
     const uint64_t scale2 = f2_pack(p.scale, p.scale);
     const int swz = kr & 7;
-    float* my_lse2 = s_lse2 + 32 * g;
-    float* my_dsum = s_dsum + 32 * g;
-    // Threads 0-31 of the group carry one lse2 value, threads 32-63 one D value,
-    // fetched from global memory one step ahead so the load latency never sits
-    // on a step's critical path.  Queries past the end: lse2 = +inf (P = 0), D = 0.
+    float* my_lse2 = s_lse2 + 64 * g;
+    float* my_dsum = s_dsum + 64 * g;
+    // Thread kr < 64 carries the lse2 of query kr of the group's slice, thread
+    // kr >= 64 its D; fetched one step ahead.  Queries past the end: lse2 = +inf
+    // (so P = 0) and D = 0.
     auto fetch = [&](int n) -> float {
-      const int qg = q_begin + n * 64 + 32 * g + (kr & 31);
-      if (kr >= 64 || n >= n_steps) return 0.f;
-      if (qg >= seq_len) return kr < 32 ? INFINITY : 0.f;
-      return kr < 32 ? p.lse2[row_base + qg] : p.dsum[row_base + qg];
+      const int qg = q_begin + n * 128 + 64 * g + (kr & 63);
+      if (n >= n_steps) return 0.f;
+      if (qg >= seq_len) return kr < 64 ? INFINITY : 0.f;
+      return kr < 64 ? p.lse2[row_base + qg] : p.dsum[row_base + qg];
     };
     float pf = fetch(0);
     bool ok = true;
     for (int n = 0; n < n_steps; ++n) {
-      const int bb = n & 1;
-      const int q0 = q_begin + n * 64 + 32 * g;  // first query of this group's slice
+      const int qs = q_begin + n * 128 + 64 * g;  // first query of the group's slice
       asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory");
-      if (kr < 32)
+      if (kr < 64)
         my_lse2[kr] = pf;
-      else if (kr < 64)
-        my_dsum[kr - 32] = pf;
+      else
+        my_dsum[kr - 64] = pf;
       asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory");
       pf = fetch(n + 1);
       // After an abort the warp keeps taking part in the named barriers and does nothing else.
       if (!ok) continue;
-      ok = mbar_wait(BAR(SD_FULL + bb), (n >> 1) & 1, w, 57) &&
-           (n < 2 || mbar_wait(BAR(DQ_FULL + bb), ((n - 2) >> 1) & 1, w, 58));  // dS^T buffer free
+      ok = mbar_wait(BAR(S_FULL), n & 1, w, 57) &&
+           (n == 0 || mbar_wait(BAR(DQ_FULL), (n - 1) & 1, w, 58));  // dS^T buffer free again
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         continue;
       }
       tc_fence_after();
-      const bool diag = CAUSAL && (q0 < k0 + 127);
-      const uint32_t tSb = tmem + lane_off + 64u * bb + 32u * g;
-      const uint32_t tDPb = tmem + lane_off + 128u + 64u * bb + 32u * g;
-      uint32_t sr[32], dr[32];
-      tmem_ld16(tSb, sr);
-      tmem_ld16(tSb + 16, sr + 16);
-      tmem_ld16(tDPb, dr);
-      tmem_ld16(tDPb + 16, dr + 16);
-      tmem_ld_wait();
-      uint32_t pp[16], dd[16];
+      const bool diag = CAUSAL && (qs < k0 + 127);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const float4* l4 = reinterpret_cast<const float4*>(my_lse2 + 16 * c);
-        const float4* d4 = reinterpret_cast<const float4*>(my_dsum + 16 * c);
+      for (int r = 0; r < 2; ++r) {
+        const uint32_t col = 64u * g + 32u * r;  // S^T / dP^T columns of this quarter
+        uint32_t sr[32], dr[32];
+        tmem_ld16(tmem + lane_off + col, sr);
+        tmem_ld16(tmem + lane_off + col + 16, sr + 16);
+        if (r == 0) {  // dP^T lands after S^T
+          ok = mbar_wait(BAR(DP_FULL), n & 1, w, 61);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        tmem_ld16(tmem + lane_off + 128 + col, dr);
+        tmem_ld16(tmem + lane_off + 128 + col + 16, dr + 16);
+        tmem_ld_wait();
+        uint32_t pp[16], dd[16];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const float4 lv = l4[q4], dv = d4[q4];
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const float4 lv = reinterpret_cast<const float4*>(my_lse2 + 32 * r)[q4];
+          const float4 dv = reinterpret_cast<const float4*>(my_dsum + 32 * r)[q4];
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
-            const int e = 16 * c + 4 * q4 + 2 * h2;  // element pair (e, e+1) of the slice
+            const int e = 4 * q4 + 2 * h2;  // element pair (e, e+1) of the quarter
             const float la = h2 ? lv.z : lv.x, lb = h2 ? lv.w : lv.y;
             const float da = h2 ? dv.z : dv.x, db = h2 ? dv.w : dv.y;
             float y0, y1;
@@ -749,30 +742,30 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
               p1 = 0.f;
             }
             if (diag) {
-              const int qg = q0 + e;
+              const int qg = qs + 32 * r + e;
               if (kg > qg) p0 = 0.f;
               if (kg > qg + 1) p1 = 0.f;
             }
-            const uint64_t pv = f2_pack(p0, p1);
             const uint64_t t = f2_add(f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), f2_pack(-da, -db));
             float g0, g1;
-            f2_unpack(f2_mul(f2_mul(pv, scale2), t), g0, g1);
+            f2_unpack(f2_mul(f2_mul(f2_pack(p0, p1), scale2), t), g0, g1);
             pp[e / 2] = pack_bf16x2(p0, p1);
             dd[e / 2] = pack_bf16x2(g0, g1);
           }
         }
-      }
-      tmem_st8(tSb, pp);  // queries 32g .. 32g+15
-      tmem_st8(tSb + 8, pp + 8);
-      uint8_t* ds_row = sbase + L::kDS0 + bb * L::kDSBytes + kr * 128;
+        const uint32_t pcol = 64u * g + 16u * r;  // P^T over this group's already-read S^T columns
+        tmem_st8(tmem + lane_off + pcol, pp);
+        tmem_st8(tmem + lane_off + pcol + 8, pp + 8);
+        uint8_t* ds_row = sbase + L::kDS + g * CHUNK + kr * 128;
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        *reinterpret_cast<uint4*>(ds_row + (((4 * g + u) ^ swz) << 4)) =
-            make_uint4(dd[4 * u], dd[4 * u + 1], dd[4 * u + 2], dd[4 * u + 3]);
-      tmem_st_wait();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(BAR(P_READY + bb));
+        for (int u = 0; u < 4; ++u)
+          *reinterpret_cast<uint4*>(ds_row + (((4 * r + u) ^ swz) << 4)) =
+              make_uint4(dd[4 * u], dd[4 * u + 1], dd[4 * u + 2], dd[4 * u + 3]);
+        tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(BAR(P_READY + 2 * r + g));
+      }
     }
     // ------------------------------------------------------------ epilogue: group 0 writes dV, group 1 dK
     if (ok) {
@@ -799,27 +792,31 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
       }
     }
   } else if (warp >= 12) {
-    // ============================================================ dQ drain (thread = one of the d rows of dQ^T)
+    // ============================================================ dQ drain (thread = one d row of dQ^T)
     const int qw = warp & 3;
     const int dr = qw * 32 + lane;
-    const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
+    const uint32_t src = tmem + ((uint32_t)(qw * 32) << 16) + 128;
     float* acc = p.dq_acc + row_base * D + dr;  // [B*H][rows][d]: a warp's lanes cover 128 contiguous bytes
     for (int n = 0; n < n_steps; ++n) {
-      const int bb = n & 1;
-      const int q0 = q_begin + n * 64;
-      bool ok = mbar_wait(BAR(DQ_FULL + bb), (n >> 1) & 1, w, 60);
+      const int q0 = q_begin + n * 128;
+      const int nq = min(128, seq_len - q0);
+      bool ok = mbar_wait(BAR(DQ_FULL), n & 1, w, 60);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      uint32_t v[64];
-      tmem_ld32(tmem + lane_off + 64u * bb, *reinterpret_cast<uint32_t(*)[32]>(v));
-      tmem_ld32(tmem + lane_off + 64u * bb + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(BAR(DQ_EMPTY + bb));  // the columns are free for S^T of step n+2
-      const int nq = min(64, seq_len - q0);
 #pragma unroll
-      for (int j = 0; j < 64; ++j)
-        if (j < nq) atomicAdd(acc + (size_t)(q0 + j) * D, __uint_as_float(v[j]));
+      for (int half = 0; half < 2; ++half) {
+        uint32_t v[64];
+        tmem_ld32(src + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(v));
+        tmem_ld32(src + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+        tmem_ld_wait();
+        if (half == 1) {
+          tc_fence_before();
+          mbar_arrive(BAR(DQ_EMPTY));  // the columns are free for the next dP^T
+        }
+#pragma unroll
+        for (int j = 0; j < 64; ++j)
+          if (64 * half + j < nq) atomicAdd(acc + (size_t)(q0 + 64 * half + j) * D, __uint_as_float(v[j]));
+      }
     }
   }
 
