@@ -474,7 +474,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 //   group's own, already-read S^T columns.
 //   Shared: K_j, V_j 32 KB each; two stages of Q_i, dO_i (32 KB each);
 //           dS^T 128 keys x 128 queries (two 64-query chunks).
-constexpr int kBwd128Threads = 512;
+// Warps: 0-3 and 12-15 drain dQ^T (query columns 0-63 and 64-127), 4-11
+// recompute P and dS, 16 issues TMA loads, 17 owns TMEM and issues the MMAs.
+constexpr int kBwd128Threads = 576;
+constexpr int kWarpProducer = 16;
+constexpr int kWarpMma = 17;
 
 struct Bwd128Layout {
   static constexpr uint32_t kTile = 128u * 128u * 2u;  // 128 rows x 128 d
@@ -544,13 +548,13 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
     mbar_init(BAR(DP_FULL), 1);
     for (int i = 0; i < 4; ++i) mbar_init(BAR(P_READY + i), 128);
     mbar_init(BAR(DQ_FULL), 1);
-    mbar_init(BAR(DQ_EMPTY), 128);
+    mbar_init(BAR(DQ_EMPTY), 256);
     mbar_init(BAR(DKV_FINAL), 1);
     mbar_init(BAR(DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == kWarpMma) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -563,7 +567,7 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
   const uint32_t sK = base + L::kK, sV = base + L::kV, sDS = base + L::kDS;
   auto stage_q = [&](int st) -> uint32_t { return base + L::kStage0 + (uint32_t)st * L::kStageBytes; };
 
-  if (warp == 0) {
+  if (warp == kWarpProducer) {
     // ============================================================ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -593,7 +597,7 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
         }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == kWarpMma) {
     // ============================================================ MMA issuer
     if (lane == 0) {
       constexpr uint32_t IDESC_SD = idesc_bf16(128, 128, false, false);  // S^T, dP^T: M keys, N queries
@@ -791,39 +795,37 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
         }
       }
     }
-  } else if (warp >= 12) {
+  } else {
     // ============================================================ dQ drain (thread = one d row of dQ^T)
+    // warps 0-3 take query columns 0-63, warps 12-15 columns 64-127; each
+    // releases its columns right after reading them, before its atomics
+    const int half = warp >= 12 ? 1 : 0;
     const int qw = warp & 3;
     const int dr = qw * 32 + lane;
-    const uint32_t src = tmem + ((uint32_t)(qw * 32) << 16) + 128;
+    const uint32_t src = tmem + ((uint32_t)(qw * 32) << 16) + 128 + 64 * half;
     float* acc = p.dq_acc + row_base * D + dr;  // [B*H][rows][d]: a warp's lanes cover 128 contiguous bytes
     for (int n = 0; n < n_steps; ++n) {
-      const int q0 = q_begin + n * 128;
-      const int nq = min(128, seq_len - q0);
+      const int q0 = q_begin + n * 128 + 64 * half;
+      const int nq = min(64, seq_len - q0);
       bool ok = mbar_wait(BAR(DQ_FULL), n & 1, w, 60);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
+      uint32_t v[64];
+      tmem_ld32(src, *reinterpret_cast<uint32_t(*)[32]>(v));
+      tmem_ld32(src + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(BAR(DQ_EMPTY));  // the columns are free for the next dP^T
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t v[64];
-        tmem_ld32(src + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(v));
-        tmem_ld32(src + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-        tmem_ld_wait();
-        if (half == 1) {
-          tc_fence_before();
-          mbar_arrive(BAR(DQ_EMPTY));  // the columns are free for the next dP^T
-        }
-#pragma unroll
-        for (int j = 0; j < 64; ++j)
-          if (64 * half + j < nq) atomicAdd(acc + (size_t)(q0 + 64 * half + j) * D, __uint_as_float(v[j]));
-      }
+      for (int j = 0; j < 64; ++j)
+        if (j < nq) atomicAdd(acc + (size_t)(q0 + j) * D, __uint_as_float(v[j]));
     }
   }
 
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
