@@ -687,7 +687,7 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
       const int qg = q_begin + n * 128 + 64 * g + (kr & 63);
       if (n >= n_steps) return 0.f;
       if (qg >= seq_len) return kr < 64 ? INFINITY : 0.f;
-      return kr < 64 ? p.lse2[row_base + qg] : p.dsum[row_base + qg];
+      return kr < 64 ? p.lse2[row_base + qg] : p.scale * p.dsum[row_base + qg];  // D staged as scale * D
     };
     float pf = fetch(0);
     bool ok = true;
@@ -710,6 +710,7 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
       }
       tc_fence_after();
       const bool diag = CAUSAL && (qs < k0 + 127);
+      const bool tail_rows = k0 + 128 > seq_len;  // only the last key block has rows past the end
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         const uint32_t col = 64u * g + 32u * r;  // S^T / dP^T columns of this quarter
@@ -741,7 +742,7 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
             f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl2x2, f2_pack(-la, -lb)),
                       y0, y1);
             float p0 = ex2_sfu(y0), p1 = ex2_sfu(y1);
-            if (!row_ok) {
+            if (tail_rows && !row_ok) {
               p0 = 0.f;
               p1 = 0.f;
             }
@@ -750,9 +751,10 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
               if (kg > qg) p0 = 0.f;
               if (kg > qg + 1) p1 = 0.f;
             }
-            const uint64_t t = f2_add(f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), f2_pack(-da, -db));
+            // dS = P * (scale * dP - scale * D): one packed FMA and one packed multiply
+            const uint64_t t = f2_fma(f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), scale2, f2_pack(-da, -db));
             float g0, g1;
-            f2_unpack(f2_mul(f2_mul(f2_pack(p0, p1), scale2), t), g0, g1);
+            f2_unpack(f2_mul(f2_pack(p0, p1), t), g0, g1);
             pp[e / 2] = pack_bf16x2(p0, p1);
             dd[e / 2] = pack_bf16x2(g0, g1);
           }
