@@ -675,19 +675,18 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
     const int kg = k0 + kr;
     const bool row_ok = kg < seq_len;
     const uint32_t lane_off = (uint32_t)(kw * 32) << 16;
-    const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
-    const uint64_t scale2 = f2_pack(p.scale, p.scale);
     const int swz = kr & 7;
     float* my_lse2 = s_lse2 + 64 * g;
     float* my_dsum = s_dsum + 64 * g;
-    // Thread kr < 64 carries the lse2 of query kr of the group's slice, thread
-    // kr >= 64 its D; fetched one step ahead.  Queries past the end: lse2 = +inf
-    // (so P = 0) and D = 0.
+    // Thread kr < 64 carries -lse2 of query kr of the group's slice, thread
+    // kr >= 64 its -scale * D; fetched one step ahead.  Queries past the end:
+    // -lse2 = -inf (so P = 0) and D = 0.
     auto fetch = [&](int n) -> float {
       const int qg = q_begin + n * 128 + 64 * g + (kr & 63);
       if (n >= n_steps) return 0.f;
-      if (qg >= seq_len) return kr < 64 ? INFINITY : 0.f;
-      return kr < 64 ? p.lse2[row_base + qg] : p.scale * p.dsum[row_base + qg];  // D staged as scale * D
+      if (qg >= seq_len) return kr < 64 ? -INFINITY : 0.f;
+      // staged negated, so each feeds an FMA as the addend: -lse2 and -scale * D
+      return kr < 64 ? -p.lse2[row_base + qg] : -p.scale * p.dsum[row_base + qg];
     };
     float pf = fetch(0);
     bool ok = true;
@@ -711,62 +710,64 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
       tc_fence_after();
       const bool diag = CAUSAL && (qs < k0 + 127);
       const bool tail_rows = k0 + 128 > seq_len;  // only the last key block has rows past the end
+      const float sl2 = p.scale_log2, scale = p.scale;
+      uint8_t* ds_row = sbase + L::kDS + g * CHUNK + kr * 128;
+#pragma unroll 1
+      for (int r = 0; r < 2; ++r) {  // quarter: 32 queries, handled as two runs of 16
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const uint32_t col = 64u * g + 32u * r;  // S^T / dP^T columns of this quarter
-        uint32_t sr[32], dr[32];
-        tmem_ld16(tmem + lane_off + col, sr);
-        tmem_ld16(tmem + lane_off + col + 16, sr + 16);
-        if (r == 0) {  // dP^T lands after S^T
-          ok = mbar_wait(BAR(DP_FULL), n & 1, w, 61);
-          if (!__all_sync(0xffffffffu, ok)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-        }
-        tmem_ld16(tmem + lane_off + 128 + col, dr);
-        tmem_ld16(tmem + lane_off + 128 + col + 16, dr + 16);
-        tmem_ld_wait();
-        uint32_t pp[16], dd[16];
-#pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) {
-          const float4 lv = reinterpret_cast<const float4*>(my_lse2 + 32 * r)[q4];
-          const float4 dv = reinterpret_cast<const float4*>(my_dsum + 32 * r)[q4];
-#pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const int e = 4 * q4 + 2 * h2;  // element pair (e, e+1) of the quarter
-            const float la = h2 ? lv.z : lv.x, lb = h2 ? lv.w : lv.y;
-            const float da = h2 ? dv.z : dv.x, db = h2 ? dv.w : dv.y;
-            float y0, y1;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl2x2, f2_pack(-la, -lb)),
-                      y0, y1);
-            float p0 = ex2_sfu(y0), p1 = ex2_sfu(y1);
-            if (tail_rows && !row_ok) {
-              p0 = 0.f;
-              p1 = 0.f;
+        for (int hh = 0; hh < 2; ++hh) {
+          const uint32_t col = 64u * g + 32u * r + 16u * hh;  // S^T / dP^T columns of this run
+          uint32_t sr[16], dr[16];
+          tmem_ld16(tmem + lane_off + col, sr);
+          if (r == 0 && hh == 0) {  // dP^T lands after S^T
+            ok = mbar_wait(BAR(DP_FULL), n & 1, w, 61);
+            if (!__all_sync(0xffffffffu, ok)) {
+              ok = false;
+              break;
             }
-            if (diag) {
-              const int qg = qs + 32 * r + e;
-              if (kg > qg) p0 = 0.f;
-              if (kg > qg + 1) p1 = 0.f;
-            }
-            // dS = P * (scale * dP - scale * D): one packed FMA and one packed multiply
-            const uint64_t t = f2_fma(f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), scale2, f2_pack(-da, -db));
-            float g0, g1;
-            f2_unpack(f2_mul(f2_pack(p0, p1), t), g0, g1);
-            pp[e / 2] = pack_bf16x2(p0, p1);
-            dd[e / 2] = pack_bf16x2(g0, g1);
+            tc_fence_after();
           }
-        }
-        const uint32_t pcol = 64u * g + 16u * r;  // P^T over this group's already-read S^T columns
-        tmem_st8(tmem + lane_off + pcol, pp);
-        tmem_st8(tmem + lane_off + pcol + 8, pp + 8);
-        uint8_t* ds_row = sbase + L::kDS + g * CHUNK + kr * 128;
+          tmem_ld16(tmem + lane_off + 128 + col, dr);
+          tmem_ld_wait();
+          const float4* nl4 = reinterpret_cast<const float4*>(my_lse2 + 32 * r + 16 * hh);  // -lse2
+          const float4* nd4 = reinterpret_cast<const float4*>(my_dsum + 32 * r + 16 * hh);  // -scale * D
+          // P = 2^(s * scale * log2 e - lse2)
+          float pv[16];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          *reinterpret_cast<uint4*>(ds_row + (((4 * r + u) ^ swz) << 4)) =
-              make_uint4(dd[4 * u], dd[4 * u + 1], dd[4 * u + 2], dd[4 * u + 3]);
+          for (int e4 = 0; e4 < 4; ++e4) {
+            const float4 nl = nl4[e4];
+            pv[4 * e4 + 0] = ex2_sfu(fmaf(__uint_as_float(sr[4 * e4 + 0]), sl2, nl.x));
+            pv[4 * e4 + 1] = ex2_sfu(fmaf(__uint_as_float(sr[4 * e4 + 1]), sl2, nl.y));
+            pv[4 * e4 + 2] = ex2_sfu(fmaf(__uint_as_float(sr[4 * e4 + 2]), sl2, nl.z));
+            pv[4 * e4 + 3] = ex2_sfu(fmaf(__uint_as_float(sr[4 * e4 + 3]), sl2, nl.w));
+          }
+          if (diag || (tail_rows && !row_ok)) {  // masks in a separate, warp-uniform pass
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              if (!row_ok || (diag && kg > qs + 32 * r + 16 * hh + e)) pv[e] = 0.f;
+          }
+          // dS = P * (scale * dP - scale * D)
+          uint32_t pp[8], dd[8];
+#pragma unroll
+          for (int e4 = 0; e4 < 4; ++e4) {
+            const float4 nd = nd4[e4];
+            const float g0 = pv[4 * e4 + 0] * fmaf(__uint_as_float(dr[4 * e4 + 0]), scale, nd.x);
+            const float g1 = pv[4 * e4 + 1] * fmaf(__uint_as_float(dr[4 * e4 + 1]), scale, nd.y);
+            const float g2 = pv[4 * e4 + 2] * fmaf(__uint_as_float(dr[4 * e4 + 2]), scale, nd.z);
+            const float g3 = pv[4 * e4 + 3] * fmaf(__uint_as_float(dr[4 * e4 + 3]), scale, nd.w);
+            pp[2 * e4] = pack_bf16x2(pv[4 * e4 + 0], pv[4 * e4 + 1]);
+            pp[2 * e4 + 1] = pack_bf16x2(pv[4 * e4 + 2], pv[4 * e4 + 3]);
+            dd[2 * e4] = pack_bf16x2(g0, g1);
+            dd[2 * e4 + 1] = pack_bf16x2(g2, g3);
+          }
+          // P^T over this group's already-read S^T columns: query q at column 64*(q/64) + (q%64)/2
+          tmem_st8(tmem + lane_off + 64u * g + 16u * r + 8u * hh, pp);
+          // dS^T row kr, 16 queries = two 16-byte units of the 128-byte swizzled row
+          const int unit = 4 * r + 2 * hh;
+          *reinterpret_cast<uint4*>(ds_row + ((unit ^ swz) << 4)) = make_uint4(dd[0], dd[1], dd[2], dd[3]);
+          *reinterpret_cast<uint4*>(ds_row + (((unit + 1) ^ swz) << 4)) = make_uint4(dd[4], dd[5], dd[6], dd[7]);
+        }
+        if (!ok) break;
         tmem_st_wait();
         fence_proxy_async_smem();
         tc_fence_before();
