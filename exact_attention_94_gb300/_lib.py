@@ -10,6 +10,7 @@ LIB_PATH = os.path.join(HERE, "libfa.so")
 (FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_MISALIGNED, FA_ERR_LAUNCH, FA_ERR_TIMEOUT,
  FA_ERR_SCRATCH_LIMIT) = range(7)
 FA_BWD_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+FA_DEVERR_SELFTEST_CODE = 0x10FF
 FA_OPT_RESCALE_TAU, FA_OPT_POLY_EXP, FA_OPT_WAIT_TIMEOUT_MS = 1, 2, 3
 
 # every symbol include/fa.h declares, with (restype, argtypes)
@@ -30,6 +31,7 @@ SIGNATURES = {
     "fa_decode_num_splits": (_I, [_I, _I, _I, _I]),
     "fa_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _F, _P]),
     "fa_device_error": (_I, [ctypes.POINTER(ctypes.c_uint)]),
+    "fa_selftest_wait_timeout": (_I, [ctypes.c_double, _P]),
     "fa_set_option": (_I, [_I, ctypes.c_double]),
 }
 

@@ -3,6 +3,7 @@
 // every entry point.
 #include "../../include/fa.h"
 #include "fa_internal.h"
+#include "ptx.cuh"
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -16,6 +17,22 @@
 namespace fa {
 
 __device__ unsigned int g_fa_error = 0;
+constexpr unsigned kSelftestSite = 0xFFu;
+
+// Self-test of the bounded wait: one warp waits on an mbarrier that nothing
+// ever arrives on, through the same helper every kernel uses.
+__global__ void fa_wait_selftest_kernel(unsigned* err, unsigned long long timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const WaitCtx w{&abort_flag, timeout_ns, err};
+  mbar_wait(smem_u32(&bar), 0, w, kSelftestSite);
+}
 
 namespace {
 
@@ -101,6 +118,13 @@ fa_status fa_set_option(fa_option opt, double value) {
       return FA_OK;
   }
   return FA_ERR_INVALID_ARG;
+}
+
+fa_status fa_selftest_wait_timeout(double timeout_ms, fa_stream_t stream) {
+  if (!(timeout_ms >= 1.0 && timeout_ms <= 10000.0)) return FA_ERR_INVALID_ARG;
+  if (!ensure_init()) return FA_ERR_LAUNCH;
+  fa_wait_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(g_err_ptr, (unsigned long long)(timeout_ms * 1e6));
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 fa_status fa_device_error(unsigned int* code) {

@@ -192,6 +192,17 @@ fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_ca
 fa_status fa_device_error(unsigned int* code);
 
 /*
+ * Failure-detection self-test: launches one warp that waits, through the same
+ * bounded-wait helper every kernel uses, on a barrier nothing ever arrives on.
+ * The wait gives up after timeout_ms (1 .. 10000) and records
+ * FA_DEVERR_SELFTEST_CODE, so a following fa_device_error() returns
+ * FA_ERR_TIMEOUT with that code and the context stays usable.  The pages have
+ * no counterpart; this checks the library's guard against hung waits.
+ */
+#define FA_DEVERR_SELFTEST_CODE 0x10FFu
+fa_status fa_selftest_wait_timeout(double timeout_ms, fa_stream_t stream);
+
+/*
  * Developer knobs (process-wide; they change speed, not results beyond
  * rounding):
  *   FA_OPT_RESCALE_TAU   : lazy-rescale threshold in log2 units (default 8;
