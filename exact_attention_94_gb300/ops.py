@@ -76,15 +76,21 @@ def fwd(q, k, v, causal: bool = False, scale: Optional[float] = None, out=None, 
 
 
 def bwd(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float] = None, workspace=None,
-        stream=None):
-    """Dense backward -> (dq, dk, dv), each [B, N, H, d] bf16."""
+        stream=None, out=None):
+    """Dense backward -> (dq, dk, dv), each [B, N, H, d] bf16 (written into
+    ``out`` = (dq, dk, dv) when given)."""
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
         _check_bf16(name, t, q.shape)
     B, N, H, d = q.shape
     if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
         raise ValueError("lse must be contiguous fp32 [B, H, N]")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if out is not None:
+        dq, dk, dv = out
+        for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+            _check_bf16(name, t, q.shape)
+    else:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     nbytes = lib().fa_bwd_workspace_bytes(B, H, N, d)
     ws = workspace if workspace is not None else torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
     if ws.numel() * ws.element_size() < nbytes:
