@@ -419,6 +419,15 @@ def run_extra(peaks):
         out["decode"] = {"ms": round(t, 4), "GB/s": round(byts / t / 1e6, 1),
                          "frac_of_hbm": round(byts / t / 1e6 / peaks["hbm_gbs"], 4)}
         del x
+        torch.cuda.empty_cache()
+        # the same decode over a paged cache: 16-token pages in shuffled order
+        xp = synth.make_paged_decode([w.N] * w.B, w.H, w.d, page_size=16, seed=0, device="cuda")
+        bt, sl = xp["block_table"].cuda(), xp["seq_lens"].cuda()
+        f = lambda: ops.decode_paged(xp["q"], xp["k_pages"], xp["v_pages"], bt, sl, w.N)
+        t = time_calls(torch, f, warm=2, iters=5)
+        out["decode_paged"] = {"ms": round(t, 4), "GB/s": round(byts / t / 1e6, 1),
+                               "frac_of_hbm": round(byts / t / 1e6 / peaks["hbm_gbs"], 4), "page_size": 16}
+        del xp
     except _lib.FaError:
         pass
     torch.cuda.empty_cache()

@@ -136,7 +136,7 @@ fa_status fa_device_error(unsigned int* code) {
   if (v != 0) {
     const unsigned zero = 0;
     cudaMemcpyToSymbol(g_fa_error, &zero, sizeof(zero));
-    return FA_ERR_TIMEOUT;
+    return v >= FA_DEVERR_BAD_PAGE ? FA_ERR_INVALID_ARG : FA_ERR_TIMEOUT;
   }
   return FA_OK;
 }
@@ -338,6 +338,54 @@ int fa_decode_num_splits(int B, int H, int L, int d) {
   if (s > max_s) s = max_s;
   if (s < 1) s = 1;
   return (int)s;
+}
+
+fa_status fa_decode_paged(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
+                          const int* seq_lens, void* o, float* lse, int B, int H, int d, int page_size, int num_pages,
+                          int max_blocks, int max_seq_len, int num_splits, void* workspace, float scale,
+                          fa_stream_t stream) {
+  if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !o || !lse || !workspace) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || num_pages < 1 || max_blocks < 1 || max_seq_len < 0 || num_splits < 0)
+    return FA_ERR_INVALID_ARG;
+  if (page_size < 4 || page_size % 4 != 0 || (long long)max_blocks * page_size < max_seq_len)
+    return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k_pages, v_pages, o, lse, workspace};
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) return FA_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return FA_ERR_MISALIGNED;
+  const int S = num_splits > 0 ? num_splits : fa_decode_num_splits(B, H, max_seq_len, d);
+  if (max_seq_len > 0 && S > max_seq_len) return FA_ERR_INVALID_ARG;
+  const int G = decode_group(H);
+  if (B > 65535 || H / G > 65535) return FA_ERR_INVALID_ARG;
+  if (!ensure_init()) return FA_ERR_LAUNCH;
+  const size_t part_bytes = align256((size_t)B * H * S * d * sizeof(float));
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  DecodeParams p{};
+  p.q = q;
+  p.k = k_pages;
+  p.v = v_pages;
+  p.part_o = reinterpret_cast<float*>(ws);
+  p.part_lse = reinterpret_cast<float*>(ws + part_bytes);
+  p.B = B;
+  p.H = H;
+  p.L = max_seq_len;
+  p.G = G;
+  p.chunk = max_seq_len > 0 ? (max_seq_len + S - 1) / S : 0;
+  p.num_splits = S;
+  p.stages = decode_stages(G, d);
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.page_size = page_size;
+  p.max_blocks = max_blocks;
+  p.num_pages = num_pages;
+  p.scale_log2 = scale * kLog2e;
+  p.err = g_err_ptr;
+  p.timeout_ns = g_opt.timeout_ns;
+  cudaError_t e = launch_decode(p, d, o, lse, (cudaStream_t)stream);
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse, int B,

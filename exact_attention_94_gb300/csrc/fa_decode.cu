@@ -75,8 +75,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) fa_decode_split_kernel(const D
   const int NS = p.stages;
   const uint32_t row_bytes = (uint32_t)G * D * 2;         // one key, all heads of the group
   const uint32_t stage_bytes = 2u * kDecT * row_bytes;    // K rows then V rows
+  int L_b = p.L;  // keys of this sequence
+  if (p.seq_lens != nullptr) {
+    L_b = p.seq_lens[b];
+    if (L_b < 0 || L_b > p.L) {  // never read past what the caller described
+      if (threadIdx.x == 0) atomicCAS(p.err, 0u, FA_DEVERR_BAD_SEQLEN);
+      L_b = L_b < 0 ? 0 : p.L;
+    }
+  }
   const int l0 = c * p.chunk;
-  const int l1 = min(p.L, l0 + p.chunk);
+  const int l1 = min(L_b, l0 + p.chunk);
   const int n_keys = max(0, l1 - l0);
   const int n_st = (n_keys + kDecT - 1) / kDecT;
 
@@ -108,7 +116,18 @@ __global__ void __launch_bounds__(kDecThreads, 1) fa_decode_split_kernel(const D
         mbar_arrive_expect_tx(FULL(slot), 2u * nv * row_bytes);
         const uint32_t dk = base + slot * stage_bytes;
         for (int m = 0; m < nv; ++m) {
-          const size_t row = ((size_t)b * p.L + l0 + s * kDecT + m) * p.H * D + kv_head0;
+          const int l = l0 + s * kDecT + m;
+          size_t row;
+          if (p.block_table != nullptr) {  // paged: logical block -> physical page
+            int page = p.block_table[(size_t)b * p.max_blocks + l / p.page_size];
+            if (page < 0 || page >= p.num_pages) {  // report, and read a valid page instead
+              atomicCAS(p.err, 0u, FA_DEVERR_BAD_PAGE);
+              page = 0;
+            }
+            row = ((size_t)page * p.page_size + l % p.page_size) * p.H * D + kv_head0;
+          } else {
+            row = ((size_t)b * p.L + l) * p.H * D + kv_head0;
+          }
           bulk_load(dk + m * row_bytes, static_cast<const __nv_bfloat16*>(p.k) + row, row_bytes, FULL(slot));
           bulk_load(dk + (kDecT + m) * row_bytes, static_cast<const __nv_bfloat16*>(p.v) + row, row_bytes,
                     FULL(slot));

@@ -13,6 +13,8 @@ namespace fa {
 
 enum : unsigned {
   FA_DEVERR_TIMEOUT_BASE = 0x1000u,  // + site id
+  FA_DEVERR_BAD_PAGE = 0x2000u,      // a block-table entry outside the page pool
+  FA_DEVERR_BAD_SEQLEN = 0x2001u,    // a sequence length outside [0, max_seq_len]
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

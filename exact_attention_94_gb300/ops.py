@@ -168,3 +168,35 @@ def decode(q, k_cache, v_cache, num_splits: int = 0, scale: Optional[float] = No
                                  _ptr(ws), scale, _stream(stream))
     _lib.check(st, "fa_decode_splitkv")
     return o, l
+
+
+def decode_paged(q, k_pages, v_pages, block_table, seq_lens, max_seq_len: int, num_splits: int = 0,
+                 scale: Optional[float] = None, stream=None, workspace=None):
+    """Single-token decode over a paged cache.  q [B, 1, H, d]; pages
+    [num_pages, page_size, H, d]; block_table int32 [B, max_blocks] and
+    seq_lens int32 [B] on the device.  Returns (o [B, 1, H, d], lse [B, H])."""
+    _check_bf16("q", q)
+    B, one, H, d = q.shape
+    if one != 1:
+        raise ValueError("q must be [B, 1, H, d]")
+    _check_bf16("k_pages", k_pages)
+    num_pages, page_size = k_pages.shape[0], k_pages.shape[1]
+    if tuple(k_pages.shape) != (num_pages, page_size, H, d):
+        raise ValueError("k_pages must be [num_pages, page_size, H, d]")
+    _check_bf16("v_pages", v_pages, k_pages.shape)
+    for name, t in (("block_table", block_table), ("seq_lens", seq_lens)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
+    if block_table.dim() != 2 or block_table.shape[0] != B or tuple(seq_lens.shape) != (B,):
+        raise ValueError("block_table must be [B, max_blocks] and seq_lens [B]")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    splits = num_splits if num_splits > 0 else lib().fa_decode_num_splits(B, H, int(max_seq_len), d)
+    nbytes = lib().fa_decode_workspace_bytes(B, H, d, max(splits, 1))
+    ws = workspace if workspace is not None else torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    o = torch.empty_like(q)
+    l = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    st = lib().fa_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seq_lens), _ptr(o),
+                               _ptr(l), B, H, d, page_size, num_pages, block_table.shape[1], int(max_seq_len), splits,
+                               _ptr(ws), scale, _stream(stream))
+    _lib.check(st, "fa_decode_paged")
+    return o, l

@@ -184,10 +184,36 @@ fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_ca
                             int H, int L, int d, int num_splits, void* workspace, float scale, fa_stream_t stream);
 
 /*
+ * Single-token decode over a paged KV cache ("Paged KV caches, a preview of
+ * serving"): the cache is a pool of fixed-size pages anywhere in memory and
+ * each sequence's block table maps its logical blocks (keys 0..P-1, P..2P-1,
+ * ...) to physical pages.  The kernel gathers one page per block; everything
+ * else is the split-KV decode above.  Only the first seq_lens[b] keys of a
+ * sequence are read: slots past it in its last page are never touched.
+ *   q                : [B, 1, H, d] bf16
+ *   k_pages, v_pages : [num_pages, page_size, H, d] bf16
+ *   block_table      : int32 [B, max_blocks], DEVICE memory
+ *   seq_lens         : int32 [B], DEVICE memory, each in [0, max_seq_len]
+ *   page_size        : a multiple of 4 (16 in the pages' example)
+ *   max_seq_len      : <= max_blocks * page_size; sizes the splits
+ *   num_splits, workspace, o, lse, scale: as fa_decode_splitkv (workspace
+ *   sized with fa_decode_workspace_bytes(B, H, d, splits))
+ * A table entry outside [0, num_pages) or a length outside [0, max_seq_len]
+ * is not dereferenced: the kernel reads page 0 / clamps the length instead and
+ * a following fa_device_error() returns FA_ERR_INVALID_ARG.
+ */
+fa_status fa_decode_paged(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
+                          const int* seq_lens, void* o, float* lse, int B, int H, int d, int page_size, int num_pages,
+                          int max_blocks, int max_seq_len, int num_splits, void* workspace, float scale,
+                          fa_stream_t stream);
+
+/*
  * Synchronises the device, then returns FA_OK if no kernel of this library
  * recorded an error since the last call, FA_ERR_TIMEOUT if a bounded wait ran
- * out (the recorded code, which names the wait site, goes to *code when code
- * is not NULL).  Clears the recorded code.
+ * out (code 0x1000 + wait site), FA_ERR_INVALID_ARG if a kernel met a bad
+ * device-side argument (0x2000: block-table entry outside the page pool,
+ * 0x2001: sequence length out of range).  The recorded code goes to *code
+ * when code is not NULL.  Clears the recorded code.
  */
 fa_status fa_device_error(unsigned int* code);
 

@@ -6,5 +6,5 @@ and the CPU-baseline legs of ``bench.py``; never by the library.
 from .attention import (  # noqa: F401
     head_forward, head_probs, head_backward, forward, backward,
     varlen_forward, varlen_backward, decode_forward, decode_partials,
-    merge_partials, split_bounds, online_head_forward,
+    merge_partials, split_bounds, online_head_forward, gather_pages, paged_decode_forward,
 )

@@ -300,3 +300,34 @@ def online_head_forward(q, k, v, scale: float, causal: bool, block_c: int, tau_l
         o = np.where(l[:, None] > 0, o_acc / l[:, None], 0.0)
         lse = np.where(l > 0, np.where(np.isfinite(m_ref), m_ref, 0.0) + np.log(l), NEG_INF)
     return o, lse, rescales
+
+
+# ---------------------------------------------------------------- paged KV cache
+
+def gather_pages(pages, block_table_row, seq_len: int):
+    """One sequence's cache from a page pool ("Paged KV caches, a preview of
+    serving"): logical block j of page_size keys lives in physical page
+    block_table_row[j]; only the first seq_len keys belong to the sequence (the
+    rest of its last page are unused slots).  pages [num_pages, P, H, d]."""
+    P = pages.shape[1]
+    n_blocks = -(-seq_len // P)
+    rows = [pages[int(block_table_row[j])] for j in range(n_blocks)]
+    if not rows:
+        return np.zeros((0,) + pages.shape[2:])
+    return np.concatenate(rows, axis=0)[:seq_len]
+
+
+def paged_decode_forward(q, k_pages, v_pages, block_table, seq_lens, scale: float):
+    """Decode against paged caches: each sequence attends to exactly its own
+    seq_len keys.  q [B, 1, H, d] -> (o [B, 1, H, d], lse [B, H])."""
+    B, _, H, d = q.shape
+    o = np.zeros((B, 1, H, v_pages.shape[-1]))
+    lse = np.zeros((B, H))
+    for b in range(B):
+        kb = gather_pages(k_pages, block_table[b], int(seq_lens[b]))
+        vb = gather_pages(v_pages, block_table[b], int(seq_lens[b]))
+        for h in range(H):
+            oh, lh = head_forward(q[b, :, h], kb[:, h], vb[:, h], scale, False)
+            o[b, 0, h] = oh[0] if len(oh) else 0.0
+            lse[b, h] = lh[0]
+    return o, lse

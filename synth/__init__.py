@@ -149,3 +149,31 @@ def make_workload(w: Workload, device="cpu", with_do=True):
 def to_f64(t: torch.Tensor):
     """Exact upcast of bf16 values to a float64 numpy array (host copy)."""
     return t.detach().to("cpu").to(torch.float64).numpy()
+
+
+def make_paged_decode(lengths, H, d, page_size=16, spare_pages=3, seed=0, device="cpu"):
+    """A paged cache for a decode batch: each sequence b gets ceil(L_b / page_size)
+    pages drawn without replacement from a shuffled pool (plus spare pages
+    nobody owns); block_table rows are padded with page 0.  Page contents,
+    including unused slots, are N(0,1) bf16 like every other input.
+    Returns q [B,1,H,d], k_pages/v_pages [num_pages, page_size, H, d],
+    block_table int32 [B, max_blocks], seq_lens int32 [B]."""
+    lengths = [int(x) for x in lengths]
+    B = len(lengths)
+    blocks = [-(-L // page_size) for L in lengths]
+    max_blocks = max(1, max(blocks))
+    num_pages = sum(blocks) + spare_pages
+    perm = torch.randperm(num_pages, generator=_gen(seed, IDX_LENGTHS, "cpu"))
+    table = torch.zeros((B, max_blocks), dtype=torch.int32)
+    nxt = 0
+    for b in range(B):
+        for j in range(blocks[b]):
+            table[b, j] = int(perm[nxt])
+            nxt += 1
+    return {
+        "q": randn_bf16((B, 1, H, d), seed, IDX_Q, device),
+        "k_pages": randn_bf16((num_pages, page_size, H, d), seed, IDX_K, device),
+        "v_pages": randn_bf16((num_pages, page_size, H, d), seed, IDX_V, device),
+        "block_table": table,
+        "seq_lens": torch.tensor(lengths, dtype=torch.int32),
+    }

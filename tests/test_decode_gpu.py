@@ -91,3 +91,53 @@ def test_decode_workload_sampled_heads():
         assert_lse(lse[b, h].cpu().numpy(), lh[0], f"decode b{b} h{h}")
     del x
     torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------- paged KV cache
+
+def run_paged(lengths, H, d, page_size, num_splits, seed=0):
+    x = synth.make_paged_decode(lengths, H, d, page_size=page_size, seed=seed)
+    dev = {n: x[n].cuda() for n in x}
+    o, lse = ops.decode_paged(dev["q"], dev["k_pages"], dev["v_pages"], dev["block_table"], dev["seq_lens"],
+                              max(lengths), num_splits=num_splits)
+    torch.cuda.synchronize()
+    return x, o, lse
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("page_size", [16, 32])
+@pytest.mark.parametrize("num_splits", [0, 1, 3])
+def test_paged_decode_ragged(d, page_size, num_splits):
+    lengths = [1, 15, 16, 17, 100, 1000]
+    x, o, lse = run_paged(lengths, 4, d, page_size, num_splits, seed=page_size)
+    assert ops.device_error() == 0
+    o_ref, l_ref = oracle.paged_decode_forward(synth.to_f64(x["q"]), synth.to_f64(x["k_pages"]),
+                                               synth.to_f64(x["v_pages"]), x["block_table"].numpy(),
+                                               x["seq_lens"].tolist(), 1.0 / math.sqrt(d))
+    assert_o(synth.to_f64(o), o_ref, f"paged O d{d} P{page_size} S{num_splits}")
+    assert_lse(lse.cpu().numpy(), l_ref, f"paged lse d{d} P{page_size} S{num_splits}")
+
+
+def test_paged_in_order_equals_contiguous_decode():
+    """Pages laid out in order with full lengths give the contiguous path's bits."""
+    B, H, L, d, P = 3, 8, 512, 128, 16
+    x = synth.make_decode(B, H, L, d, seed=21)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    table = torch.arange(B * L // P, dtype=torch.int32, device="cuda").view(B, L // P)
+    lens = torch.full((B,), L, dtype=torch.int32, device="cuda")
+    o1, l1 = ops.decode(q, k, v, num_splits=4)
+    o2, l2 = ops.decode_paged(q, k.view(B * L // P, P, H, d), v.view(B * L // P, P, H, d), table, lens, L,
+                              num_splits=4)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_paged_bad_table_entry_is_reported_not_read():
+    lengths = [40, 20]
+    x = synth.make_paged_decode(lengths, 2, 64, page_size=16, seed=5)
+    bt = x["block_table"].clone()
+    bt[1, 0] = 10_000_000  # far outside the pool
+    dev = {n: x[n].cuda() for n in x}
+    ops.decode_paged(dev["q"], dev["k_pages"], dev["v_pages"], bt.cuda(), dev["seq_lens"], max(lengths))
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0x2000
+    assert ops.device_error() == 0
