@@ -142,8 +142,9 @@ fa_status fa_device_error(unsigned int* code) {
 }
 
 static fa_status fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu,
-                            int nbatch, int n_rows, int seq_len, int max_len, int H, int d, int causal, float scale,
-                            fa_stream_t stream) {
+                            int nbatch, int n_rows, int seq_len, int max_len, int H, int Hkv, int d, int causal,
+                            float scale, fa_stream_t stream) {
+  if (Hkv < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if (!scale_ok(scale) || (causal != 0 && causal != 1)) return FA_ERR_INVALID_ARG;
@@ -155,10 +156,11 @@ static fa_status fwd_common(const void* q, const void* k, const void* v, void* o
   if (!ensure_init()) return FA_ERR_LAUNCH;
   CUtensorMap tq, tk, tv;
   const int tb = cu ? 1 : nbatch;
-  if (!make_tmap_bhnd(&tq, q, d, n_rows, H, tb) || !make_tmap_bhnd(&tk, k, d, n_rows, H, tb) ||
-      !make_tmap_bhnd(&tv, v, d, n_rows, H, tb))
+  if (!make_tmap_bhnd(&tq, q, d, n_rows, H, tb) || !make_tmap_bhnd(&tk, k, d, n_rows, Hkv, tb) ||
+      !make_tmap_bhnd(&tv, v, d, n_rows, Hkv, tb))
     return FA_ERR_INVALID_ARG;
   FwdParams p{};
+  p.kv_group = H / Hkv;
   p.o = o;
   p.lse = lse;
   p.cu_seqlens = cu;
@@ -179,7 +181,15 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  int causal, float scale, fa_stream_t stream) {
   if (B < 1 || H < 1 || N < 0) return FA_ERR_INVALID_ARG;
   if (N == 0) return FA_OK;
-  return fwd_common(q, k, v, o, lse, nullptr, B, N, N, N, H, d, causal, scale, stream);
+  return fwd_common(q, k, v, o, lse, nullptr, B, N, N, N, H, H, d, causal, scale, stream);
+}
+
+fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
+                     int d, int causal, float scale, fa_stream_t stream) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || N < 0) return FA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (N == 0) return FA_OK;
+  return fwd_common(q, k, v, o, lse, nullptr, B, N, N, N, Hq, Hkv, d, causal, scale, stream);
 }
 
 fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
@@ -188,7 +198,7 @@ fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, fl
   if (num_seqs < 1 || H < 1 || max_seqlen < 0 || total_tokens < 0 || !cu_seqlens) return FA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0) return FA_ERR_MISALIGNED;
   if (total_tokens == 0 || max_seqlen == 0) return FA_OK;
-  return fwd_common(q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, 0, max_seqlen, H, d, causal, scale,
+  return fwd_common(q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, 0, max_seqlen, H, H, d, causal, scale,
                     stream);
 }
 
@@ -207,8 +217,9 @@ size_t fa_bwd_varlen_workspace_bytes(int total_tokens, int H, int d) {
 
 static fa_status bwd_common(const void* q, const void* k, const void* v, const void* o, const float* lse,
                             const void* dout, void* dq, void* dk, void* dv, void* workspace, const int* cu,
-                            int nbatch, int n_rows, int seq_len, int max_len, int H, int d, int causal,
+                            int nbatch, int n_rows, int seq_len, int max_len, int H, int Hkv, int d, int causal,
                             float scale, fa_stream_t stream) {
+  if (Hkv < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if (!scale_ok(scale) || (causal != 0 && causal != 1)) return FA_ERR_INVALID_ARG;
@@ -222,8 +233,8 @@ static fa_status bwd_common(const void* q, const void* k, const void* v, const v
   const int tb = cu ? 1 : nbatch;
   CUtensorMap tq, tk, tv, tdo;
   const int q_box = 128;
-  if (!make_tmap_bhnd(&tq, q, d, n_rows, H, tb, q_box) || !make_tmap_bhnd(&tk, k, d, n_rows, H, tb) ||
-      !make_tmap_bhnd(&tv, v, d, n_rows, H, tb) || !make_tmap_bhnd(&tdo, dout, d, n_rows, H, tb, q_box))
+  if (!make_tmap_bhnd(&tq, q, d, n_rows, H, tb, q_box) || !make_tmap_bhnd(&tk, k, d, n_rows, Hkv, tb) ||
+      !make_tmap_bhnd(&tv, v, d, n_rows, Hkv, tb) || !make_tmap_bhnd(&tdo, dout, d, n_rows, H, tb, q_box))
     return FA_ERR_INVALID_ARG;
   const size_t acc_bytes = align256((size_t)tb * n_rows * H * d * sizeof(float));
   const size_t row_bytes = align256((size_t)tb * H * n_rows * sizeof(float));
@@ -242,6 +253,7 @@ static fa_status bwd_common(const void* q, const void* k, const void* v, const v
   p.B = nbatch;
   p.B_tensor = tb;
   p.H = H;
+  p.kv_group = H / Hkv;
   p.n_rows = n_rows;
   p.seq_len = seq_len;
   p.num_kblocks = num_kblocks;
@@ -258,7 +270,17 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  fa_stream_t stream) {
   if (B < 1 || H < 1 || N < 0) return FA_ERR_INVALID_ARG;
   if (N == 0) return FA_OK;
-  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, nullptr, B, N, N, N, H, d, causal, scale, stream);
+  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, nullptr, B, N, N, N, H, H, d, causal, scale,
+                    stream);
+}
+
+fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                     void* dq, void* dk, void* dv, void* workspace, int B, int Hq, int Hkv, int N, int d, int causal,
+                     float scale, fa_stream_t stream) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || N < 0 || Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (N == 0) return FA_OK;
+  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, nullptr, B, N, N, N, Hq, Hkv, d, causal, scale,
+                    stream);
 }
 
 fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -269,7 +291,7 @@ fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void*
   if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0) return FA_ERR_MISALIGNED;
   if (total_tokens == 0 || max_seqlen == 0) return FA_OK;
   return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, cu_seqlens, num_seqs, total_tokens, 0,
-                    max_seqlen, H, d, causal, scale, stream);
+                    max_seqlen, H, H, d, causal, scale, stream);
 }
 
 // ---------------------------------------------------------------- backward without allocation
@@ -309,7 +331,7 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
   }
   // The pre-kernel of the backward zeroes the accumulator part of the scratch
   // and overwrites the per-row arrays, so the previous call's contents never leak.
-  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, scratch, nullptr, B, N, N, N, H, d, causal, scale, stream);
+  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, scratch, nullptr, B, N, N, N, H, H, d, causal, scale, stream);
 }
 
 size_t fa_decode_workspace_bytes(int B, int H, int d, int num_splits) {
@@ -319,19 +341,19 @@ size_t fa_decode_workspace_bytes(int B, int H, int d, int num_splits) {
   return ((po + 255) & ~(size_t)255) + ((pl + 255) & ~(size_t)255);
 }
 
-// Heads handled by one decode CTA: the largest divisor of H that is at most 32.
-static int decode_group(int H) {
-  for (int g = H < 32 ? H : 32; g > 1; --g)
-    if (H % g == 0) return g;
+// K/V heads handled by one decode CTA: the largest divisor G of Hkv whose
+// query heads (G * group) fit the CTA's 32 query-head slots.
+static int decode_group(int Hkv, int group) {
+  for (int g = Hkv < 32 ? Hkv : 32; g > 1; --g)
+    if (Hkv % g == 0 && g * group <= 32) return g;
   return 1;
 }
 
-int fa_decode_num_splits(int B, int H, int L, int d) {
-  (void)d;
-  if (B < 1 || H < 1 || L <= 0) return 1;
+static int auto_splits(int B, int Hkv, int group, int L) {
+  if (B < 1 || Hkv < 1 || L <= 0) return 1;
   int dev = 0, n_sm = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-  const long long ctas_per_split = (long long)B * (H / decode_group(H));
+  const long long ctas_per_split = (long long)B * (Hkv / decode_group(Hkv, group));
   // about eight full waves of one CTA per SM, and at least 256 keys per split
   long long s = (8LL * n_sm + ctas_per_split - 1) / ctas_per_split;
   const long long max_s = (L + 255) / 256;
@@ -340,40 +362,46 @@ int fa_decode_num_splits(int B, int H, int L, int d) {
   return (int)s;
 }
 
-fa_status fa_decode_paged(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
-                          const int* seq_lens, void* o, float* lse, int B, int H, int d, int page_size, int num_pages,
-                          int max_blocks, int max_seq_len, int num_splits, void* workspace, float scale,
-                          fa_stream_t stream) {
-  if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !o || !lse || !workspace) return FA_ERR_INVALID_ARG;
-  if (B < 1 || H < 1 || num_pages < 1 || max_blocks < 1 || max_seq_len < 0 || num_splits < 0)
-    return FA_ERR_INVALID_ARG;
-  if (page_size < 4 || page_size % 4 != 0 || (long long)max_blocks * page_size < max_seq_len)
-    return FA_ERR_INVALID_ARG;
+int fa_decode_num_splits(int B, int H, int L, int d) {
+  (void)d;
+  return auto_splits(B, H, 1, L);
+}
+
+// Common decode path: contiguous cache (block_table == nullptr) or paged cache.
+static fa_status decode_common(const void* q, const void* k, const void* v, const int* block_table,
+                               const int* seq_lens, int page_size, int num_pages, int max_blocks, void* o, float* lse,
+                               int B, int H, int Hkv, int L, int d, int num_splits, void* workspace, float scale,
+                               fa_stream_t stream) {
+  if (!q || !o || !lse || !workspace) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || Hkv < 1 || H % Hkv != 0 || L < 0 || num_splits < 0) return FA_ERR_INVALID_ARG;
+  const int group = H / Hkv;
+  if (group > 32) return FA_ERR_UNSUPPORTED;  // a CTA serves at most 32 query heads
+  if (L > 0 && (!k || !v)) return FA_ERR_INVALID_ARG;  // an empty contiguous cache may be null
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
-  const void* ptrs[] = {q, k_pages, v_pages, o, lse, workspace};
+  const void* ptrs[] = {q, k, v, o, lse, workspace};
   for (const void* ptr : ptrs)
     if (!aligned16(ptr)) return FA_ERR_MISALIGNED;
-  if ((reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
-    return FA_ERR_MISALIGNED;
-  const int S = num_splits > 0 ? num_splits : fa_decode_num_splits(B, H, max_seq_len, d);
-  if (max_seq_len > 0 && S > max_seq_len) return FA_ERR_INVALID_ARG;
-  const int G = decode_group(H);
-  if (B > 65535 || H / G > 65535) return FA_ERR_INVALID_ARG;
+  const int S = num_splits > 0 ? num_splits : auto_splits(B, Hkv, group, L);
+  if (L > 0 && S > L) return FA_ERR_INVALID_ARG;
+  const int G = decode_group(Hkv, group);
+  if (B > 65535 || Hkv / G > 65535) return FA_ERR_INVALID_ARG;
   if (!ensure_init()) return FA_ERR_LAUNCH;
   const size_t part_bytes = align256((size_t)B * H * S * d * sizeof(float));
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   DecodeParams p{};
   p.q = q;
-  p.k = k_pages;
-  p.v = v_pages;
+  p.k = k;
+  p.v = v;
   p.part_o = reinterpret_cast<float*>(ws);
   p.part_lse = reinterpret_cast<float*>(ws + part_bytes);
   p.B = B;
   p.H = H;
-  p.L = max_seq_len;
+  p.Hkv = Hkv;
+  p.kv_group = group;
+  p.L = L;
   p.G = G;
-  p.chunk = max_seq_len > 0 ? (max_seq_len + S - 1) / S : 0;
+  p.chunk = L > 0 ? (L + S - 1) / S : 0;
   p.num_splits = S;
   p.stages = decode_stages(G, d);
   p.block_table = block_table;
@@ -388,41 +416,30 @@ fa_status fa_decode_paged(const void* q, const void* k_pages, const void* v_page
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
+fa_status fa_decode_paged(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
+                          const int* seq_lens, void* o, float* lse, int B, int H, int d, int page_size, int num_pages,
+                          int max_blocks, int max_seq_len, int num_splits, void* workspace, float scale,
+                          fa_stream_t stream) {
+  if (!k_pages || !v_pages || !block_table || !seq_lens) return FA_ERR_INVALID_ARG;
+  if (num_pages < 1 || max_blocks < 1 || max_seq_len < 0) return FA_ERR_INVALID_ARG;
+  if (page_size < 4 || page_size % 4 != 0 || (long long)max_blocks * page_size < max_seq_len)
+    return FA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return FA_ERR_MISALIGNED;
+  return decode_common(q, k_pages, v_pages, block_table, seq_lens, page_size, num_pages, max_blocks, o, lse, B, H, H,
+                       max_seq_len, d, num_splits, workspace, scale, stream);
+}
+
 fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse, int B,
                             int H, int L, int d, int num_splits, void* workspace, float scale, fa_stream_t stream) {
-  if (!q || !o || !lse || !workspace) return FA_ERR_INVALID_ARG;
-  if (B < 1 || H < 1 || L < 0 || num_splits < 0) return FA_ERR_INVALID_ARG;
-  if (L > 0 && (!k_cache || !v_cache)) return FA_ERR_INVALID_ARG;  // an empty cache may be null
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
-  const void* ptrs[] = {q, k_cache, v_cache, o, lse, workspace};
-  for (const void* ptr : ptrs)
-    if (!aligned16(ptr)) return FA_ERR_MISALIGNED;
-  const int S = num_splits > 0 ? num_splits : fa_decode_num_splits(B, H, L, d);
-  if (L > 0 && S > L) return FA_ERR_INVALID_ARG;
-  const int G = decode_group(H);
-  if (B > 65535 || H / G > 65535) return FA_ERR_INVALID_ARG;
-  if (!ensure_init()) return FA_ERR_LAUNCH;
-  const size_t part_bytes = align256((size_t)B * H * S * d * sizeof(float));
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  DecodeParams p{};
-  p.q = q;
-  p.k = k_cache;
-  p.v = v_cache;
-  p.part_o = reinterpret_cast<float*>(ws);
-  p.part_lse = reinterpret_cast<float*>(ws + part_bytes);
-  p.B = B;
-  p.H = H;
-  p.L = L;
-  p.G = G;
-  p.chunk = L > 0 ? (L + S - 1) / S : 0;
-  p.num_splits = S;
-  p.stages = decode_stages(G, d);
-  p.scale_log2 = scale * kLog2e;
-  p.err = g_err_ptr;
-  p.timeout_ns = g_opt.timeout_ns;
-  cudaError_t e = launch_decode(p, d, o, lse, (cudaStream_t)stream);
-  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+  return decode_common(q, k_cache, v_cache, nullptr, nullptr, 0, 0, 0, o, lse, B, H, H, L, d, num_splits, workspace,
+                       scale, stream);
+}
+
+fa_status fa_decode_gqa(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse, int B, int Hq,
+                        int Hkv, int L, int d, int num_splits, void* workspace, float scale, fa_stream_t stream) {
+  return decode_common(q, k_cache, v_cache, nullptr, nullptr, 0, 0, 0, o, lse, B, Hq, Hkv, L, d, num_splits,
+                       workspace, scale, stream);
 }
 
 }  // extern "C"

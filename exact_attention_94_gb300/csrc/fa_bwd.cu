@@ -161,10 +161,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int lane = lane_id();
 
   // ---------------------------------------------------------------- work item
+  // one CTA per (batch, K/V head, key block); with grouped-query attention it
+  // walks the query blocks of every query head that shares this K/V head
+  const int Hkv = p.H / p.kv_group;
   const int bh = (int)(blockIdx.z * gridDim.x + blockIdx.x);
-  if (bh >= p.B * p.H) return;
-  const int b = bh / p.H;
-  const int h = bh % p.H;
+  if (bh >= p.B * Hkv) return;
+  const int b = bh / Hkv;
+  const int h_kv = bh % Hkv;
   const int jb = (int)blockIdx.y;  // key block; ascending = heaviest first when causal
   int seq_start = 0, seq_len = p.seq_len, b_coord = b;
   if (p.cu_seqlens != nullptr) {
@@ -176,8 +179,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (k0 >= seq_len) return;
   const int n_qblk = (seq_len + 127) / 128;
   const int i_begin = CAUSAL ? jb : 0;
-  const int n_steps = n_qblk - i_begin;
-  const size_t row_base = (size_t)(b_coord * p.H + h) * p.n_rows + seq_start;  // lse2 / dsum / acc row origin
+  const int n_q = n_qblk - i_begin;       // query blocks per query head
+  const int n_steps = p.kv_group * n_q;   // step n: query head hq(n), query block i_begin + n % n_q
+  auto hq_of = [&](int n) { return h_kv * p.kv_group + n / n_q; };
+  auto row_base_of = [&](int hq) { return (size_t)(b_coord * p.H + hq) * p.n_rows + seq_start; };  // lse2 / dsum / acc
 
   // ---------------------------------------------------------------- barriers
   enum { KV_FULL = 0, Q_FULL = 1, STAGE_EMPTY = 3, S_FULL = 5, DP_FULL, P_READY, DQ_FULL, DQ_EMPTY, DS_EMPTY,
@@ -228,19 +233,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tma_prefetch_desc(&tm_do);
       mbar_arrive_expect_tx(BAR(KV_FULL), 2 * TILE);
       for (int c = 0; c < CH; ++c) {
-        tma_load_4d(sK + c * CHUNK, &tm_k, BAR(KV_FULL), c * 64, seq_start + k0, h, b_coord);
-        tma_load_4d(sV + c * CHUNK, &tm_v, BAR(KV_FULL), c * 64, seq_start + k0, h, b_coord);
+        tma_load_4d(sK + c * CHUNK, &tm_k, BAR(KV_FULL), c * 64, seq_start + k0, h_kv, b_coord);
+        tma_load_4d(sV + c * CHUNK, &tm_v, BAR(KV_FULL), c * 64, seq_start + k0, h_kv, b_coord);
       }
       bool ok = true;
       for (int n = 0; n < n_steps && ok; ++n) {
         const int st = n & 1;
-        const int row = seq_start + (i_begin + n) * 128;
+        const int row = seq_start + (i_begin + n % n_q) * 128;
+        const int hq = hq_of(n);
         if (n >= 2 && !(ok = mbar_wait(BAR(STAGE_EMPTY + st), ((n >> 1) - 1) & 1, w, 21))) break;
         mbar_arrive_expect_tx(BAR(Q_FULL + st), 2 * TILE);
         const uint32_t qa = stage_q(st);
         for (int c = 0; c < CH; ++c) {
-          tma_load_4d(qa + c * CHUNK, &tm_q, BAR(Q_FULL + st), c * 64, row, h, b_coord);
-          tma_load_4d(qa + TILE + c * CHUNK, &tm_do, BAR(Q_FULL + st), c * 64, row, h, b_coord);
+          tma_load_4d(qa + c * CHUNK, &tm_q, BAR(Q_FULL + st), c * 64, row, hq, b_coord);
+          tma_load_4d(qa + TILE + c * CHUNK, &tm_do, BAR(Q_FULL + st), c * 64, row, hq, b_coord);
         }
       }
       if (!ok) {
@@ -323,15 +329,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // this thread's lse2 and D of the next query block, fetched one step ahead
     // (invalid rows: lse2 = +inf, so P = 0)
     auto fetch = [&](int n, float& l2, float& ds) {
-      const int qg = (i_begin + n) * 128 + kr;
+      const int qg = (i_begin + n % n_q) * 128 + kr;
       const bool qv = n < n_steps && qg < seq_len;
-      l2 = qv ? p.lse2[row_base + qg] : INFINITY;
-      ds = qv ? p.dsum[row_base + qg] : 0.f;
+      const size_t rb = n < n_steps ? row_base_of(hq_of(n)) : 0;
+      l2 = qv ? p.lse2[rb + qg] : INFINITY;
+      ds = qv ? p.dsum[rb + qg] : 0.f;
     };
     float pf_l, pf_d;
     fetch(0, pf_l, pf_d);
     for (int n = 0; n < n_steps; ++n) {
-      const int q0 = (i_begin + n) * 128;
+      const int q0 = (i_begin + n % n_q) * 128;
       asm volatile("bar.sync 1, 128;" ::: "memory");
       s_lse2[kr] = pf_l;
       s_dsum[kr] = pf_d;
@@ -399,7 +406,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = mbar_wait(BAR(DKV_FINAL), 0, w, 29);
       if (__all_sync(0xffffffffu, ok)) {
         tc_fence_after();
-        const size_t grow = ((size_t)b_coord * p.n_rows + seq_start + kg) * p.H + h;
+        const size_t grow = ((size_t)b_coord * p.n_rows + seq_start + kg) * Hkv + h_kv;
         __nv_bfloat16* dv_row = reinterpret_cast<__nv_bfloat16*>(p.dv) + grow * D;
         __nv_bfloat16* dk_row = reinterpret_cast<__nv_bfloat16*>(p.dk) + grow * D;
 #pragma unroll
@@ -428,9 +435,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int qw = warp & 3;
     const int r = qw * 32 + lane;
     const uint32_t tDQ = tmem + ((uint32_t)(qw * 32) << 16) + 128;
-    float4* acc = reinterpret_cast<float4*>(p.dq_acc) + (size_t)(b_coord * p.H + h) * (D / 4) * p.n_rows;
     for (int n = 0; n < n_steps; ++n) {
-      const int qg = (i_begin + n) * 128 + r;
+      float4* acc = reinterpret_cast<float4*>(p.dq_acc) + (size_t)(b_coord * p.H + hq_of(n)) * (D / 4) * p.n_rows;
+      const int qg = (i_begin + n % n_q) * 128 + r;
       bool ok = mbar_wait(BAR(DQ_FULL), n & 1, w, 30);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
@@ -511,10 +518,13 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
   const int warp = warp_id();
   const int lane = lane_id();
 
+  // one CTA per (batch, K/V head, key block); with grouped-query attention it
+  // walks the query blocks of every query head that shares this K/V head
+  const int Hkv = p.H / p.kv_group;
   const int bh = (int)(blockIdx.z * gridDim.x + blockIdx.x);
-  if (bh >= p.B * p.H) return;
-  const int b = bh / p.H;
-  const int h = bh % p.H;
+  if (bh >= p.B * Hkv) return;
+  const int b = bh / Hkv;
+  const int h_kv = bh % Hkv;
   const int jb = (int)blockIdx.y;
   int seq_start = 0, seq_len = p.seq_len, b_coord = b;
   if (p.cu_seqlens != nullptr) {
@@ -525,8 +535,10 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
   const int k0 = jb * 128;
   if (k0 >= seq_len) return;
   const int q_begin = CAUSAL ? k0 : 0;
-  const int n_steps = (seq_len - q_begin + 127) / 128;
-  const size_t row_base = (size_t)(b_coord * p.H + h) * p.n_rows + seq_start;
+  const int n_q = (seq_len - q_begin + 127) / 128;  // query blocks per query head
+  const int n_steps = p.kv_group * n_q;              // step n: query head hq(n), block n % n_q
+  auto hq_of = [&](int n) { return h_kv * p.kv_group + n / n_q; };
+  auto row_base_of = [&](int hq) { return (size_t)(b_coord * p.H + hq) * p.n_rows + seq_start; };
 
   enum { KV_FULL = 0, Q_FULL = 1, STAGE_EMPTY = Q_FULL + NST, S_FULL = STAGE_EMPTY + NST, DP_FULL = S_FULL + 1,
          P_READY = DP_FULL + 1,
@@ -576,19 +588,20 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
       tma_prefetch_desc(&tm_do);
       mbar_arrive_expect_tx(BAR(KV_FULL), 2 * L::kTile);
       for (int c = 0; c < 2; ++c) {
-        tma_load_4d(sK + c * CHUNK, &tm_k, BAR(KV_FULL), c * 64, seq_start + k0, h, b_coord);
-        tma_load_4d(sV + c * CHUNK, &tm_v, BAR(KV_FULL), c * 64, seq_start + k0, h, b_coord);
+        tma_load_4d(sK + c * CHUNK, &tm_k, BAR(KV_FULL), c * 64, seq_start + k0, h_kv, b_coord);
+        tma_load_4d(sV + c * CHUNK, &tm_v, BAR(KV_FULL), c * 64, seq_start + k0, h_kv, b_coord);
       }
       bool ok = true;
       for (int n = 0; n < n_steps && ok; ++n) {
         const int st = n % NST;
-        const int row = seq_start + q_begin + n * 128;
+        const int row = seq_start + q_begin + (n % n_q) * 128;
+        const int hq = hq_of(n);
         if (n >= NST && !(ok = mbar_wait(BAR(STAGE_EMPTY + st), ((n / NST) - 1) & 1, w, 51))) break;
         mbar_arrive_expect_tx(BAR(Q_FULL + st), 2 * L::kTile);
         const uint32_t qa = stage_q(st);
         for (int c = 0; c < 2; ++c) {
-          tma_load_4d(qa + c * CHUNK, &tm_q, BAR(Q_FULL + st), c * 64, row, h, b_coord);
-          tma_load_4d(qa + L::kTile + c * CHUNK, &tm_do, BAR(Q_FULL + st), c * 64, row, h, b_coord);
+          tma_load_4d(qa + c * CHUNK, &tm_q, BAR(Q_FULL + st), c * 64, row, hq, b_coord);
+          tma_load_4d(qa + L::kTile + c * CHUNK, &tm_do, BAR(Q_FULL + st), c * 64, row, hq, b_coord);
         }
       }
       if (!ok) {
@@ -682,8 +695,9 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
     // kr >= 64 its -scale * D; fetched one step ahead.  Queries past the end:
     // -lse2 = -inf (so P = 0) and D = 0.
     auto fetch = [&](int n) -> float {
-      const int qg = q_begin + n * 128 + 64 * g + (kr & 63);
       if (n >= n_steps) return 0.f;
+      const int qg = q_begin + (n % n_q) * 128 + 64 * g + (kr & 63);
+      const size_t row_base = row_base_of(hq_of(n));
       if (qg >= seq_len) return kr < 64 ? -INFINITY : 0.f;
       // staged negated, so each feeds an FMA as the addend: -lse2 and -scale * D
       return kr < 64 ? -p.lse2[row_base + qg] : -p.scale * p.dsum[row_base + qg];
@@ -691,7 +705,7 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
     float pf = fetch(0);
     bool ok = true;
     for (int n = 0; n < n_steps; ++n) {
-      const int qs = q_begin + n * 128 + 64 * g;  // first query of the group's slice
+      const int qs = q_begin + (n % n_q) * 128 + 64 * g;  // first query of the group's slice
       asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory");
       if (kr < 64)
         my_lse2[kr] = pf;
@@ -779,7 +793,7 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
       ok = mbar_wait(BAR(DKV_FINAL), 0, w, 59);
       if (__all_sync(0xffffffffu, ok)) {
         tc_fence_after();
-        const size_t grow = ((size_t)b_coord * p.n_rows + seq_start + kg) * p.H + h;
+        const size_t grow = ((size_t)b_coord * p.n_rows + seq_start + kg) * Hkv + h_kv;
         const uint32_t src = tmem + lane_off + (g ? 384u : 256u);
         __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(g ? p.dk : p.dv) + grow * D;
 #pragma unroll
@@ -806,9 +820,9 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
     const int qw = warp & 3;
     const int dr = qw * 32 + lane;
     const uint32_t src = tmem + ((uint32_t)(qw * 32) << 16) + 128 + 64 * half;
-    float* acc = p.dq_acc + row_base * D + dr;  // [B*H][rows][d]: a warp's lanes cover 128 contiguous bytes
     for (int n = 0; n < n_steps; ++n) {
-      const int q0 = q_begin + n * 128 + 64 * half;
+      float* acc = p.dq_acc + row_base_of(hq_of(n)) * D + dr;  // [B*H][rows][d]: a warp's lanes cover 128 bytes
+      const int q0 = q_begin + (n % n_q) * 128 + 64 * half;
       const int nq = min(64, seq_len - q0);
       bool ok = mbar_wait(BAR(DQ_FULL), n & 1, w, 60);
       if (!__all_sync(0xffffffffu, ok)) break;
@@ -852,7 +866,7 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const int bh = p.B * p.H;
+  const int bh = p.B * (p.H / p.kv_group);  // CTAs walk (batch, K/V head) pairs
   const int gx = bh < kBwdHeadGroup ? bh : kBwdHeadGroup;
   dim3 grid(gx, p.num_kblocks, (bh + gx - 1) / gx);
   kern<<<grid, D == 128 ? kBwd128Threads : kBwdThreads, smem, stream>>>(tq, tk, tv, tdo, p);

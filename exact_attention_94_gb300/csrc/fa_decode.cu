@@ -70,8 +70,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) fa_decode_split_kernel(const D
   const int lane = lane_id();
   const int c = blockIdx.x;   // chunk
   const int b = blockIdx.y;   // batch entry
-  const int hg = blockIdx.z;  // head group
-  const int G = p.G;
+  const int hg = blockIdx.z;  // group of K/V heads
+  const int G = p.G;                 // K/V heads of this CTA
+  const int Gq = G * p.kv_group;     // query heads of this CTA (those K/V heads' groups)
   const int NS = p.stages;
   const uint32_t row_bytes = (uint32_t)G * D * 2;         // one key, all heads of the group
   const uint32_t stage_bytes = 2u * kDecT * row_bytes;    // K rows then V rows
@@ -124,9 +125,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) fa_decode_split_kernel(const D
               atomicCAS(p.err, 0u, FA_DEVERR_BAD_PAGE);
               page = 0;
             }
-            row = ((size_t)page * p.page_size + l % p.page_size) * p.H * D + kv_head0;
+            row = ((size_t)page * p.page_size + l % p.page_size) * p.Hkv * D + kv_head0;
           } else {
-            row = ((size_t)b * p.L + l) * p.H * D + kv_head0;
+            row = ((size_t)b * p.L + l) * p.Hkv * D + kv_head0;
           }
           bulk_load(dk + m * row_bytes, static_cast<const __nv_bfloat16*>(p.k) + row, row_bytes, FULL(slot));
           bulk_load(dk + (kDecT + m) * row_bytes, static_cast<const __nv_bfloat16*>(p.v) + row, row_bytes,
@@ -149,9 +150,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) fa_decode_split_kernel(const D
       l_lane[j] = 0.f;
 #pragma unroll
       for (int e = 0; e < E; ++e) o[j][e] = 0.f;
-      if (hj < G) {
+      if (hj < Gq) {
         const __nv_bfloat16* qs =
-            static_cast<const __nv_bfloat16*>(p.q) + ((size_t)b * p.H + hg * G + hj) * D + lane * E;
+            static_cast<const __nv_bfloat16*>(p.q) + ((size_t)b * p.H + hg * Gq + hj) * D + lane * E;
         load_row<E>(qs, qv[j]);
 #pragma unroll
         for (int e = 0; e < E; ++e) qv[j][e] *= p.scale_log2;  // scores come out in log2 units
@@ -172,14 +173,15 @@ __global__ void __launch_bounds__(kDecThreads, 1) fa_decode_split_kernel(const D
       const __nv_bfloat16* vs = ks + kDecT * G * D;
 #pragma unroll
       for (int j = 0; j < kDecHPW; ++j) {
-        const int hj = warp + kDecWarps * j;
-        if (hj >= G) break;
+        const int hj = warp + kDecWarps * j;  // query head of the CTA
+        if (hj >= Gq) break;
+        const int kvj = hj / p.kv_group;      // its K/V head of the CTA
         // partial dot products of this lane's elements for the 4 keys
         float part[kDecT];
 #pragma unroll
         for (int m = 0; m < kDecT; ++m) {
           float kf[E];
-          load_row<E>(ks + ((size_t)m * G + hj) * D + lane * E, kf);
+          load_row<E>(ks + ((size_t)m * G + kvj) * D + lane * E, kf);
           float acc = 0.f;
 #pragma unroll
           for (int e = 0; e < E; ++e) acc = fmaf(qv[j][e], kf[e], acc);
@@ -209,7 +211,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) fa_decode_split_kernel(const D
           if (m < nv) {
             const float pk = __shfl_sync(0xffffffffu, pm, (m >> 1) * 16 + (m & 1) * 8);
             float vf[E];
-            load_row<E>(vs + ((size_t)m * G + hj) * D + lane * E, vf);
+            load_row<E>(vs + ((size_t)m * G + kvj) * D + lane * E, vf);
 #pragma unroll
             for (int e = 0; e < E; ++e) o[j][e] = fmaf(pk, vf[e], o[j][e]);
           }
@@ -223,10 +225,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) fa_decode_split_kernel(const D
 #pragma unroll
       for (int j = 0; j < kDecHPW; ++j) {
         const int hj = warp + kDecWarps * j;
-        if (hj >= G) break;
+        if (hj >= Gq) break;
         float l = l_lane[j] + __shfl_xor_sync(0xffffffffu, l_lane[j], 8);
         l += __shfl_xor_sync(0xffffffffu, l, 16);
-        const size_t pidx = ((size_t)b * p.H + hg * G + hj) * p.num_splits + c;
+        const size_t pidx = ((size_t)b * p.H + hg * Gq + hj) * p.num_splits + c;
         const float inv = l > 0.f ? 1.f / l : 0.f;
         float* dst = p.part_o + pidx * D + lane * E;
 #pragma unroll
@@ -293,7 +295,7 @@ static cudaError_t launch_decode_t(const DecodeParams& p, void* o, float* lse, c
   const size_t smem = decode_smem_bytes(p.G, D);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.num_splits, p.B, p.H / p.G);
+  dim3 grid(p.num_splits, p.B, p.Hkv / p.G);
   kern<<<grid, kDecThreads, smem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -91,6 +91,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (bh >= p.bh_total) return;
   const int b = bh / p.H;
   const int h = bh % p.H;
+  const int h_kv = h / p.kv_group;  // grouped-query attention: K/V head shared by kv_group query heads
   const int pair = p.num_pairs - 1 - (int)blockIdx.y;  // heaviest causal pairs first
   int seq_start = 0, seq_len = p.seq_len, b_coord = b;
   if (p.cu_seqlens != nullptr) {
@@ -174,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(BAR(KV_FULL + slot), TILE);
           const CUtensorMap* m = which ? &tm_v : &tm_k;
           for (int c = 0; c < CH; ++c)
-            tma_load_4d(kv_s + slot * TILE + c * CHUNK, m, BAR(KV_FULL + slot), c * 64, seq_start + 128 * j, h,
+            tma_load_4d(kv_s + slot * TILE + c * CHUNK, m, BAR(KV_FULL + slot), c * 64, seq_start + 128 * j, h_kv,
                         b_coord);
         }
       }

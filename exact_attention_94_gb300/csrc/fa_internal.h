@@ -13,7 +13,8 @@ struct FwdParams {
   void* o;                   // bf16 output
   float* lse;                // fp32 log-sum-exp
   const int* cu_seqlens;     // packed batch offsets (device) or nullptr for a dense batch
-  int H;
+  int H;                     // query heads
+  int kv_group;              // query heads per K/V head (grouped-query attention; 1 = one K/V head per query head)
   int bh_total;              // (batch or sequences) * H
   int n_rows;                // rows along the sequence axis of the tensors (N, or total tokens)
   int seq_len;               // dense: N
@@ -37,7 +38,8 @@ struct BwdParams {
   const int* cu_seqlens;     // packed batch offsets (device) or nullptr
   int B;                     // dense batch, or number of sequences
   int B_tensor;              // leading extent of the tensors: B (dense) or 1 (packed)
-  int H;
+  int H;                     // query heads
+  int kv_group;              // query heads per K/V head (1 = one K/V head per query head)
   int n_rows;                // rows along the sequence axis of the tensors
   int seq_len;               // dense: N
   int num_kblocks;           // grid.y of the main kernel
@@ -64,9 +66,11 @@ struct DecodeParams {
   float* part_o;             // [B, H, num_splits, d] fp32: each chunk's normalised output
   float* part_lse;           // [B, H, num_splits] fp32: each chunk's log2 softmax mass
   int B;
-  int H;
+  int H;                     // query heads
+  int Hkv;                   // K/V heads (grouped-query attention: H = Hkv * kv_group)
+  int kv_group;
   int L;
-  int G;                     // heads per CTA (divides H, at most 32)
+  int G;                     // K/V heads per CTA (divides Hkv; G * kv_group <= 32 query heads)
   int chunk;                 // keys per split
   int num_splits;
   int stages;                // shared-memory ring depth

@@ -200,3 +200,63 @@ def decode_paged(q, k_pages, v_pages, block_table, seq_lens, max_seq_len: int, n
                                _ptr(ws), scale, _stream(stream))
     _lib.check(st, "fa_decode_paged")
     return o, l
+
+
+# ---------------------------------------------------------------- grouped-query attention
+
+def fwd_gqa(q, k, v, causal: bool = False, scale: Optional[float] = None, stream=None):
+    """q [B, N, Hq, d]; k, v [B, N, Hkv, d] with Hkv dividing Hq.
+    Returns (o [B, N, Hq, d], lse [B, Hq, N])."""
+    _check_bf16("q", q)
+    B, N, Hq, d = q.shape
+    _check_bf16("k", k)
+    Hkv = k.shape[2]
+    if tuple(k.shape) != (B, N, Hkv, d):
+        raise ValueError("k must be [B, N, Hkv, d]")
+    _check_bf16("v", v, k.shape)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q)
+    l = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    st = lib().fa_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, Hq, Hkv, N, d, int(bool(causal)), scale,
+                          _stream(stream))
+    _lib.check(st, "fa_fwd_gqa")
+    return o, l
+
+
+def bwd_gqa(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float] = None, stream=None):
+    """Gradients of fwd_gqa: (dq [B, N, Hq, d], dk, dv [B, N, Hkv, d])."""
+    for name, t in (("q", q), ("o", o), ("dout", dout)):
+        _check_bf16(name, t, q.shape)
+    B, N, Hq, d = q.shape
+    _check_bf16("k", k)
+    Hkv = k.shape[2]
+    _check_bf16("v", v, k.shape)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    nbytes = lib().fa_bwd_workspace_bytes(B, Hq, N, d)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    st = lib().fa_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                          _ptr(ws), B, Hq, Hkv, N, d, int(bool(causal)), scale, _stream(stream))
+    _lib.check(st, "fa_bwd_gqa")
+    return dq, dk, dv
+
+
+def decode_gqa(q, k_cache, v_cache, num_splits: int = 0, scale: Optional[float] = None, stream=None):
+    """q [B, 1, Hq, d]; caches [B, L, Hkv, d].  Returns (o [B, 1, Hq, d], lse [B, Hq])."""
+    _check_bf16("q", q)
+    B, one, Hq, d = q.shape
+    _check_bf16("k_cache", k_cache)
+    L, Hkv = k_cache.shape[1], k_cache.shape[2]
+    if one != 1 or tuple(k_cache.shape) != (B, L, Hkv, d):
+        raise ValueError("q must be [B, 1, Hq, d] and the caches [B, L, Hkv, d]")
+    _check_bf16("v_cache", v_cache, k_cache.shape)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    splits = num_splits if num_splits > 0 else lib().fa_decode_num_splits(B, Hkv, L, d)
+    nbytes = lib().fa_decode_workspace_bytes(B, Hq, d, max(splits, 1))
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    o = torch.empty_like(q)
+    l = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    st = lib().fa_decode_gqa(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(l), B, Hq, Hkv, L, d, splits,
+                             _ptr(ws), scale, _stream(stream))
+    _lib.check(st, "fa_decode_gqa")
+    return o, l

@@ -78,6 +78,17 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  int causal, float scale, fa_stream_t stream);
 
 /*
+ * Grouped-query attention forward ("Using it, the real way": fewer key-value
+ * heads than query heads, shared in groups).  Query head h attends with K/V
+ * head h / (Hq / Hkv).
+ *   q, o    : [B, N, Hq, d] bf16;   lse : [B, Hq, N] fp32
+ *   k, v    : [B, N, Hkv, d] bf16, Hkv divides Hq
+ * Otherwise as fa_fwd (fa_fwd is this call with Hkv = Hq).
+ */
+fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
+                     int d, int causal, float scale, fa_stream_t stream);
+
+/*
  * Scratch bytes fa_bwd needs: an fp32 dQ accumulator [B, N, H, d] and the
  * row sums D_i = sum_k dO_ik O_ik [B, H, N] fp32.
  */
@@ -97,6 +108,17 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                  void* dq, void* dk, void* dv, void* workspace, int B, int H, int N, int d, int causal, float scale,
                  fa_stream_t stream);
+
+/*
+ * Grouped-query attention backward: dK and dV of each K/V head sum the
+ * contributions of every query head in its group.
+ *   q, o, dout, dq : [B, N, Hq, d];  k, v, dk, dv : [B, N, Hkv, d];  lse [B, Hq, N]
+ *   workspace      : fa_bwd_workspace_bytes(B, Hq, N, d) bytes
+ * Otherwise as fa_bwd.
+ */
+fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                     void* dq, void* dk, void* dv, void* workspace, int B, int Hq, int Hkv, int N, int d, int causal,
+                     float scale, fa_stream_t stream);
 
 /*
  * Forward pass, packed variable-length batch ("Variable-length batches
@@ -182,6 +204,14 @@ int fa_decode_num_splits(int B, int H, int L, int d);
  */
 fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse, int B,
                             int H, int L, int d, int num_splits, void* workspace, float scale, fa_stream_t stream);
+
+/*
+ * Grouped-query single-token decode: q [B, 1, Hq, d], caches [B, L, Hkv, d]
+ * with Hkv dividing Hq and Hq / Hkv <= 32; every K/V row is read once for
+ * all the query heads of its group.  Otherwise as fa_decode_splitkv.
+ */
+fa_status fa_decode_gqa(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse, int B, int Hq,
+                        int Hkv, int L, int d, int num_splits, void* workspace, float scale, fa_stream_t stream);
 
 /*
  * Single-token decode over a paged KV cache ("Paged KV caches, a preview of

@@ -7,4 +7,5 @@ from .attention import (  # noqa: F401
     head_forward, head_probs, head_backward, forward, backward,
     varlen_forward, varlen_backward, decode_forward, decode_partials,
     merge_partials, split_bounds, online_head_forward, gather_pages, paged_decode_forward,
+    gqa_forward, gqa_backward, gqa_decode_forward,
 )

@@ -331,3 +331,51 @@ def paged_decode_forward(q, k_pages, v_pages, block_table, seq_lens, scale: floa
             o[b, 0, h] = oh[0] if len(oh) else 0.0
             lse[b, h] = lh[0]
     return o, lse
+
+
+# ---------------------------------------------------------------- grouped-query attention
+
+def gqa_forward(q, k, v, scale: float, causal: bool):
+    """Grouped-query attention ("Using it, the real way": fewer key-value heads,
+    shared in groups): query head h uses K/V head h // (Hq / Hkv).
+    q [B, N, Hq, d], k/v [B, N, Hkv, d] -> (o [B, N, Hq, d], lse [B, Hq, N])."""
+    B, N, Hq, d = q.shape
+    group = Hq // k.shape[2]
+    o = np.zeros((B, N, Hq, v.shape[-1]))
+    lse = np.zeros((B, Hq, N))
+    for b in range(B):
+        for h in range(Hq):
+            oh, lh = head_forward(q[b, :, h], k[b, :, h // group], v[b, :, h // group], scale, causal)
+            o[b, :, h] = oh
+            lse[b, h] = lh
+    return o, lse
+
+
+def gqa_backward(q, k, v, do, scale: float, causal: bool):
+    """Gradients of gqa_forward: dK and dV of a K/V head sum over its query heads."""
+    B, N, Hq, d = q.shape
+    group = Hq // k.shape[2]
+    dq = np.zeros(q.shape)
+    dk = np.zeros(k.shape)
+    dv = np.zeros(v.shape)
+    for b in range(B):
+        for h in range(Hq):
+            gq, gk, gv = head_backward(q[b, :, h], k[b, :, h // group], v[b, :, h // group], do[b, :, h], scale, causal)
+            dq[b, :, h] = gq
+            dk[b, :, h // group] += gk
+            dv[b, :, h // group] += gv
+    return dq, dk, dv
+
+
+def gqa_decode_forward(q, k_cache, v_cache, scale: float):
+    """Single-query decode with grouped K/V heads: q [B, 1, Hq, d], caches [B, L, Hkv, d]."""
+    B, _, Hq, d = q.shape
+    group = Hq // k_cache.shape[2]
+    o = np.zeros((B, 1, Hq, v_cache.shape[-1]))
+    lse = np.zeros((B, Hq))
+    for b in range(B):
+        for h in range(Hq):
+            oh, lh = head_forward(q[b, :, h], k_cache[b, :, h // group], v_cache[b, :, h // group], scale, False)
+            o[b, 0, h] = oh[0]
+            lse[b, h] = lh[0]
+    return o, lse
