@@ -9,3 +9,7 @@ from .attention import (  # noqa: F401
     merge_partials, split_bounds, online_head_forward, gather_pages, paged_decode_forward,
     gqa_forward, gqa_backward, gqa_decode_forward,
 )
+from .masked import (  # noqa: F401
+    window_visible, top_left_causal_visible, block_mask, head_forward_visible, head_backward_visible,
+    masked_forward, masked_backward, masked_varlen_forward, masked_varlen_backward,
+)

@@ -177,3 +177,34 @@ def make_paged_decode(lengths, H, d, page_size=16, spare_pages=3, seed=0, device
         "block_table": table,
         "seq_lens": torch.tensor(lengths, dtype=torch.int32),
     }
+
+
+def make_masked(B, Nq, Nk, Hq, Hkv, d, seed=0, device="cpu", with_do=True):
+    """Queries against a key/value set of another length (chunked prefill):
+    q (and dO) [B, Nq, Hq, d], k, v [B, Nk, Hkv, d], bf16."""
+    out = {
+        "q": randn_bf16((B, Nq, Hq, d), seed, IDX_Q, device),
+        "k": randn_bf16((B, Nk, Hkv, d), seed, IDX_K, device),
+        "v": randn_bf16((B, Nk, Hkv, d), seed, IDX_V, device),
+    }
+    if with_do:
+        out["do"] = randn_bf16((B, Nq, Hq, d), seed, IDX_DO, device)
+    return out
+
+
+def make_masked_varlen(lengths_q, lengths_k, Hq, Hkv, d, seed=0, device="cpu", with_do=True):
+    """Packed queries and keys with their own lengths per sequence:
+    q (and dO) [total_q, Hq, d], k, v [total_k, Hkv, d], int32 cu_seqlens_q / _k."""
+    cu_q = cu_seqlens_from_lengths(lengths_q)
+    cu_k = cu_seqlens_from_lengths(lengths_k)
+    tq, tk = int(cu_q[-1]), int(cu_k[-1])
+    out = {
+        "q": randn_bf16((tq, Hq, d), seed, IDX_Q, device),
+        "k": randn_bf16((tk, Hkv, d), seed, IDX_K, device),
+        "v": randn_bf16((tk, Hkv, d), seed, IDX_V, device),
+        "cu_seqlens_q": cu_q,
+        "cu_seqlens_k": cu_k,
+    }
+    if with_do:
+        out["do"] = randn_bf16((tq, Hq, d), seed, IDX_DO, device)
+    return out
