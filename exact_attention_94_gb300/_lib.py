@@ -30,6 +30,10 @@ SIGNATURES = {
     "fa_bwd_varlen_workspace_bytes": (_S, [_I, _I, _I]),
     "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "fa_bwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "fa_fwd_masked": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "fa_fwd_masked_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P] + [_I] * 10 + [_F, _P]),
+    "fa_bwd_masked": (_I, [_P] * 10 + [_I] * 8 + [_F, _P]),
+    "fa_bwd_masked_varlen": (_I, [_P] * 12 + [_I] * 10 + [_F, _P]),
     "fa_decode_workspace_bytes": (_S, [_I, _I, _I, _I]),
     "fa_decode_num_splits": (_I, [_I, _I, _I, _I]),
     "fa_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _F, _P]),

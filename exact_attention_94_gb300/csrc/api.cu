@@ -141,13 +141,23 @@ fa_status fa_device_error(unsigned int* code) {
   return FA_OK;
 }
 
+// Window bounds: -1 leaves a side unbounded; a bound that reaches past every
+// key of the longest sequence is the same as none, so it is dropped.
+static bool window_ok(int& wl, int& wr, int max_len_q, int max_len_k) {
+  if (wl < -1 || wr < -1) return false;
+  if (wl >= max_len_k) wl = -1;
+  if (wr >= max_len_q) wr = -1;
+  return true;
+}
+
 static fa_status fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu,
-                            int nbatch, int n_rows, int seq_len, int max_len, int H, int Hkv, int d, int causal,
-                            float scale, fa_stream_t stream) {
+                            const int* cu_k, int nbatch, int n_rows, int n_rows_k, int seq_len, int seq_len_k,
+                            int max_len, int max_len_k, int H, int Hkv, int d, int wl, int wr, float scale,
+                            fa_stream_t stream) {
   if (Hkv < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (!scale_ok(scale) || (causal != 0 && causal != 1)) return FA_ERR_INVALID_ARG;
+  if (!scale_ok(scale) || !window_ok(wl, wr, max_len, max_len_k)) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_MISALIGNED;
   if ((long long)nbatch * H > 65535LL * 8) return FA_ERR_INVALID_ARG;  // grid.z limit with 8-head groups
@@ -156,50 +166,93 @@ static fa_status fwd_common(const void* q, const void* k, const void* v, void* o
   if (!ensure_init()) return FA_ERR_LAUNCH;
   CUtensorMap tq, tk, tv;
   const int tb = cu ? 1 : nbatch;
-  if (!make_tmap_bhnd(&tq, q, d, n_rows, H, tb) || !make_tmap_bhnd(&tk, k, d, n_rows, Hkv, tb) ||
-      !make_tmap_bhnd(&tv, v, d, n_rows, Hkv, tb))
+  if (!make_tmap_bhnd(&tq, q, d, n_rows, H, tb) || !make_tmap_bhnd(&tk, k, d, n_rows_k, Hkv, tb) ||
+      !make_tmap_bhnd(&tv, v, d, n_rows_k, Hkv, tb))
     return FA_ERR_INVALID_ARG;
   FwdParams p{};
   p.kv_group = H / Hkv;
   p.o = o;
   p.lse = lse;
   p.cu_seqlens = cu;
+  p.cu_seqlens_k = cu_k;
   p.H = H;
   p.bh_total = nbatch * H;
   p.n_rows = n_rows;
+  p.n_rows_k = n_rows_k;
   p.seq_len = seq_len;
+  p.seq_len_k = seq_len_k;
+  p.win_left = wl;
+  p.win_right = wr;
   p.num_pairs = num_pairs;
   p.scale_log2 = scale * kLog2e;
   p.tau = g_opt.tau;
   p.err = g_err_ptr;
   p.timeout_ns = g_opt.timeout_ns;
-  cudaError_t e = launch_fwd(tq, tk, tv, p, d, causal != 0, g_opt.poly, nbatch * H, (cudaStream_t)stream);
+  cudaError_t e = launch_fwd(tq, tk, tv, p, d, mask_kind(wl, wr), g_opt.poly, nbatch * H, (cudaStream_t)stream);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
+// causal flag of the square entry points -> window (-1, 0), else no mask
+static int causal_right(int causal) { return causal ? 0 : -1; }
+
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
                  int causal, float scale, fa_stream_t stream) {
-  if (B < 1 || H < 1 || N < 0) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 0 || (causal != 0 && causal != 1)) return FA_ERR_INVALID_ARG;
   if (N == 0) return FA_OK;
-  return fwd_common(q, k, v, o, lse, nullptr, B, N, N, N, H, H, d, causal, scale, stream);
+  return fwd_common(q, k, v, o, lse, nullptr, nullptr, B, N, N, N, N, N, N, H, H, d, -1, causal_right(causal),
+                    scale, stream);
 }
 
 fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
                      int d, int causal, float scale, fa_stream_t stream) {
-  if (B < 1 || Hq < 1 || Hkv < 1 || N < 0) return FA_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || N < 0 || (causal != 0 && causal != 1)) return FA_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (N == 0) return FA_OK;
-  return fwd_common(q, k, v, o, lse, nullptr, B, N, N, N, Hq, Hkv, d, causal, scale, stream);
+  return fwd_common(q, k, v, o, lse, nullptr, nullptr, B, N, N, N, N, N, N, Hq, Hkv, d, -1, causal_right(causal),
+                    scale, stream);
 }
 
 fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
                         int num_seqs, int max_seqlen, int total_tokens, int H, int d, int causal, float scale,
                         fa_stream_t stream) {
   if (num_seqs < 1 || H < 1 || max_seqlen < 0 || total_tokens < 0 || !cu_seqlens) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0) return FA_ERR_MISALIGNED;
   if (total_tokens == 0 || max_seqlen == 0) return FA_OK;
-  return fwd_common(q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, 0, max_seqlen, H, H, d, causal, scale,
-                    stream);
+  return fwd_common(q, k, v, o, lse, cu_seqlens, cu_seqlens, num_seqs, total_tokens, total_tokens, 0, 0, max_seqlen,
+                    max_seqlen, H, H, d, -1, causal_right(causal), scale, stream);
+}
+
+fa_status fa_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                        int Nq, int Nk, int d, int window_left, int window_right, float scale, fa_stream_t stream) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 0 || Nk < 0 || Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (window_left < -1 || window_right < -1) return FA_ERR_INVALID_ARG;
+  if (Nq == 0) return FA_OK;
+  if (Nk == 0) {  // no keys: the kernel writes O = 0 and lse = -inf; K and V are never read
+    return fwd_common(q, q, q, o, lse, nullptr, nullptr, B, Nq, 1, Nq, 0, Nq, 1, Hq, Hq, d, -1, -1, scale,
+                      stream);
+  }
+  return fwd_common(q, k, v, o, lse, nullptr, nullptr, B, Nq, Nk, Nq, Nk, Nq, Nk, Hq, Hkv, d, window_left,
+                    window_right, scale, stream);
+}
+
+fa_status fa_fwd_masked_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                               const int* cu_seqlens_q, const int* cu_seqlens_k, int num_seqs, int max_seqlen_q,
+                               int max_seqlen_k, int total_q, int total_k, int Hq, int Hkv, int d, int window_left,
+                               int window_right, float scale, fa_stream_t stream) {
+  if (num_seqs < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || !cu_seqlens_q || !cu_seqlens_k) return FA_ERR_INVALID_ARG;
+  if (max_seqlen_q < 0 || max_seqlen_k < 0 || total_q < 0 || total_k < 0) return FA_ERR_INVALID_ARG;
+  if (window_left < -1 || window_right < -1) return FA_ERR_INVALID_ARG;
+  if (((reinterpret_cast<uintptr_t>(cu_seqlens_q) | reinterpret_cast<uintptr_t>(cu_seqlens_k)) & 3u) != 0)
+    return FA_ERR_MISALIGNED;
+  if (total_q == 0 || max_seqlen_q == 0) return FA_OK;
+  if (total_k == 0) {  // every sequence has an empty cache: O = 0 and lse = -inf
+    return fwd_common(q, q, q, o, lse, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, 1, 0, 0, max_seqlen_q, 1, Hq,
+                      Hq, d, -1, -1, scale, stream);
+  }
+  if (max_seqlen_k == 0) return FA_ERR_INVALID_ARG;
+  return fwd_common(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q, total_k, 0, 0, max_seqlen_q,
+                    max_seqlen_k, Hq, Hkv, d, window_left, window_right, scale, stream);
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -217,24 +270,25 @@ size_t fa_bwd_varlen_workspace_bytes(int total_tokens, int H, int d) {
 
 static fa_status bwd_common(const void* q, const void* k, const void* v, const void* o, const float* lse,
                             const void* dout, void* dq, void* dk, void* dv, void* workspace, const int* cu,
-                            int nbatch, int n_rows, int seq_len, int max_len, int H, int Hkv, int d, int causal,
-                            float scale, fa_stream_t stream) {
+                            const int* cu_k, int nbatch, int n_rows, int n_rows_k, int seq_len, int seq_len_k,
+                            int max_len, int max_len_k, int H, int Hkv, int d, int wl, int wr, float scale,
+                            fa_stream_t stream) {
   if (Hkv < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (!scale_ok(scale) || (causal != 0 && causal != 1)) return FA_ERR_INVALID_ARG;
+  if (!scale_ok(scale) || !window_ok(wl, wr, max_len, max_len_k)) return FA_ERR_INVALID_ARG;
   const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv, workspace};
   for (const void* ptr : ptrs)
     if (!aligned16(ptr)) return FA_ERR_MISALIGNED;
   if ((long long)nbatch * H > 65535LL * 8) return FA_ERR_INVALID_ARG;
-  const int num_kblocks = (max_len + 127) / 128;
+  const int num_kblocks = (max_len_k + 127) / 128;
   if (num_kblocks > 65535) return FA_ERR_INVALID_ARG;
   if (!ensure_init()) return FA_ERR_LAUNCH;
   const int tb = cu ? 1 : nbatch;
   CUtensorMap tq, tk, tv, tdo;
   const int q_box = 128;
-  if (!make_tmap_bhnd(&tq, q, d, n_rows, H, tb, q_box) || !make_tmap_bhnd(&tk, k, d, n_rows, Hkv, tb) ||
-      !make_tmap_bhnd(&tv, v, d, n_rows, Hkv, tb) || !make_tmap_bhnd(&tdo, dout, d, n_rows, H, tb, q_box))
+  if (!make_tmap_bhnd(&tq, q, d, n_rows, H, tb, q_box) || !make_tmap_bhnd(&tk, k, d, n_rows_k, Hkv, tb) ||
+      !make_tmap_bhnd(&tv, v, d, n_rows_k, Hkv, tb) || !make_tmap_bhnd(&tdo, dout, d, n_rows, H, tb, q_box))
     return FA_ERR_INVALID_ARG;
   const size_t acc_bytes = align256((size_t)tb * n_rows * H * d * sizeof(float));
   const size_t row_bytes = align256((size_t)tb * H * n_rows * sizeof(float));
@@ -250,37 +304,43 @@ static fa_status bwd_common(const void* q, const void* k, const void* v, const v
   p.dk = dk;
   p.dv = dv;
   p.cu_seqlens = cu;
+  p.cu_seqlens_k = cu_k;
   p.B = nbatch;
   p.B_tensor = tb;
   p.H = H;
   p.kv_group = H / Hkv;
   p.n_rows = n_rows;
+  p.n_rows_k = n_rows_k;
   p.seq_len = seq_len;
+  p.seq_len_k = seq_len_k;
+  p.win_left = wl;
+  p.win_right = wr;
   p.num_kblocks = num_kblocks;
   p.scale = scale;
   p.scale_log2 = scale * kLog2e;
   p.err = g_err_ptr;
   p.timeout_ns = g_opt.timeout_ns;
-  cudaError_t e = launch_bwd(tq, tk, tv, tdo, p, d, causal != 0, (cudaStream_t)stream);
+  cudaError_t e = launch_bwd(tq, tk, tv, tdo, p, d, mask_kind(wl, wr), (cudaStream_t)stream);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                  void* dq, void* dk, void* dv, void* workspace, int B, int H, int N, int d, int causal, float scale,
                  fa_stream_t stream) {
-  if (B < 1 || H < 1 || N < 0) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 0 || (causal != 0 && causal != 1)) return FA_ERR_INVALID_ARG;
   if (N == 0) return FA_OK;
-  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, nullptr, B, N, N, N, H, H, d, causal, scale,
-                    stream);
+  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, nullptr, nullptr, B, N, N, N, N, N, N, H, H, d,
+                    -1, causal_right(causal), scale, stream);
 }
 
 fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                      void* dq, void* dk, void* dv, void* workspace, int B, int Hq, int Hkv, int N, int d, int causal,
                      float scale, fa_stream_t stream) {
-  if (B < 1 || Hq < 1 || Hkv < 1 || N < 0 || Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || N < 0 || Hq % Hkv != 0 || (causal != 0 && causal != 1))
+    return FA_ERR_INVALID_ARG;
   if (N == 0) return FA_OK;
-  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, nullptr, B, N, N, N, Hq, Hkv, d, causal, scale,
-                    stream);
+  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, nullptr, nullptr, B, N, N, N, N, N, N, Hq, Hkv, d,
+                    -1, causal_right(causal), scale, stream);
 }
 
 fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -288,10 +348,34 @@ fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void*
                         int num_seqs, int max_seqlen, int total_tokens, int H, int d, int causal, float scale,
                         fa_stream_t stream) {
   if (num_seqs < 1 || H < 1 || max_seqlen < 0 || total_tokens < 0 || !cu_seqlens) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0) return FA_ERR_MISALIGNED;
   if (total_tokens == 0 || max_seqlen == 0) return FA_OK;
-  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, cu_seqlens, num_seqs, total_tokens, 0,
-                    max_seqlen, H, H, d, causal, scale, stream);
+  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, cu_seqlens, cu_seqlens, num_seqs, total_tokens,
+                    total_tokens, 0, 0, max_seqlen, max_seqlen, H, H, d, -1, causal_right(causal), scale, stream);
+}
+
+fa_status fa_bwd_masked(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                        const void* dout, void* dq, void* dk, void* dv, void* workspace, int B, int Hq, int Hkv,
+                        int Nq, int Nk, int d, int window_left, int window_right, float scale, fa_stream_t stream) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nk < 1 || Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (window_left < -1 || window_right < -1) return FA_ERR_INVALID_ARG;
+  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, nullptr, nullptr, B, Nq, Nk, Nq, Nk, Nq, Nk, Hq,
+                    Hkv, d, window_left, window_right, scale, stream);
+}
+
+fa_status fa_bwd_masked_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                               const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                               const int* cu_seqlens_q, const int* cu_seqlens_k, int num_seqs, int max_seqlen_q,
+                               int max_seqlen_k, int total_q, int total_k, int Hq, int Hkv, int d, int window_left,
+                               int window_right, float scale, fa_stream_t stream) {
+  if (num_seqs < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || !cu_seqlens_q || !cu_seqlens_k) return FA_ERR_INVALID_ARG;
+  if (max_seqlen_q < 1 || max_seqlen_k < 1 || total_q < 1 || total_k < 1) return FA_ERR_INVALID_ARG;
+  if (window_left < -1 || window_right < -1) return FA_ERR_INVALID_ARG;
+  if (((reinterpret_cast<uintptr_t>(cu_seqlens_q) | reinterpret_cast<uintptr_t>(cu_seqlens_k)) & 3u) != 0)
+    return FA_ERR_MISALIGNED;
+  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q,
+                    total_k, 0, 0, max_seqlen_q, max_seqlen_k, Hq, Hkv, d, window_left, window_right, scale, stream);
 }
 
 // ---------------------------------------------------------------- backward without allocation
@@ -311,7 +395,7 @@ void* g_scratch_ptr[kMaxDevices] = {};  // device address of g_bwd_scratch, per 
 fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
                          const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
                          float scale, fa_stream_t stream) {
-  if (B < 1 || H < 1 || N < 0) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 0 || (causal != 0 && causal != 1)) return FA_ERR_INVALID_ARG;
   if (N == 0) return FA_OK;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if (fa_bwd_workspace_bytes(B, H, N, d) > (size_t)FA_BWD_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_LIMIT;
@@ -331,7 +415,8 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
   }
   // The pre-kernel of the backward zeroes the accumulator part of the scratch
   // and overwrites the per-row arrays, so the previous call's contents never leak.
-  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, scratch, nullptr, B, N, N, N, H, H, d, causal, scale, stream);
+  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, scratch, nullptr, nullptr, B, N, N, N, N, N, N, H, H, d, -1,
+                    causal_right(causal), scale, stream);
 }
 
 size_t fa_decode_workspace_bytes(int B, int H, int d, int num_splits) {

@@ -7,8 +7,8 @@
 // many blocks add into the same dQ_i with atomic additions):
 //
 //   pre:   D_i = sum_c dO_ic O_ic;  lse2_i = lse_i * log2 e;  dQacc = 0
-//   main:  one CTA per 128-key block K_j, V_j; for every query block i
-//          (i >= j when causal):
+//   main:  one CTA per 128-key block K_j, V_j; for every 128-row query step i
+//          that sees a key of the block (all of them without a mask):
 //            S^T  = K_j Q_i^T                 (tcgen05, TMEM)
 //            dP^T = V_j dO_i^T                (tcgen05, TMEM)
 //            P^T  = 2^(S^T scale log2 e - lse2)       (bf16, back into TMEM)
@@ -29,6 +29,7 @@
 #include "fa_internal.h"
 #include "ptx.cuh"
 
+#include <climits>
 #include <cmath>
 
 namespace fa {
@@ -140,9 +141,75 @@ __global__ void __launch_bounds__(256) fa_bwd_post_kernel(const float* __restric
   *reinterpret_cast<uint2*>(dq + (((size_t)bt * n_rows + n) * H + h) * D + c4 * 4) = out;
 }
 
+// ---------------------------------------------------------------- work items and masks
+
+// A backward CTA owns key block [k0, k0 + 128) of one (sequence, K/V head) and
+// walks the query rows [q_lo, q_hi) that see at least one of its keys.  With
+// the bottom-right mask, query i sees keys [i + off - win_left, i + off +
+// win_right], off = kv_len - seq_len, so those rows are
+//   q_lo = k0 - off - win_right,  q_hi = k0 + 127 - off + win_left + 1
+// (clamped to [0, seq_len); an unbounded side leaves the full range).
+struct BwdItem {
+  int seq_start, seq_len;  // query rows of the sequence
+  int kv_start, kv_len;    // key rows of the sequence
+  int b_coord;             // batch coordinate of the tensors (0 when packed)
+  int off;                 // kv_len - seq_len
+  int q_lo, q_hi;
+  bool bad;                // packed offsets outside the tensors
+};
+
+template <int MASK>
+__device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int b, int k0) {
+  BwdItem it{0, p.seq_len, 0, p.seq_len_k, b, 0, 0, 0, false};
+  if (p.cu_seqlens != nullptr) {
+    it.seq_start = p.cu_seqlens[b];
+    it.seq_len = p.cu_seqlens[b + 1] - it.seq_start;
+    it.kv_start = p.cu_seqlens_k[b];
+    it.kv_len = p.cu_seqlens_k[b + 1] - it.kv_start;
+    it.b_coord = 0;
+    it.bad = it.seq_start < 0 || it.seq_len < 0 || it.seq_start > p.n_rows - it.seq_len || it.kv_start < 0 ||
+             it.kv_len < 0 || it.kv_start > p.n_rows_k - it.kv_len;
+  }
+  it.off = it.kv_len - it.seq_len;
+  it.q_lo = 0;
+  it.q_hi = it.seq_len;
+  if (MASK != kMaskNone && p.win_right >= 0) it.q_lo = max(0, k0 - it.off - p.win_right);
+  if (MASK == kMaskWindow) it.q_hi = min(it.seq_len, k0 + 128 - it.off + p.win_left);
+  return it;
+}
+
+// Query q is hidden from key kg iff q < mask_a(kg) or q > mask_b(kg).
+template <int MASK>
+__device__ __forceinline__ int mask_a(const BwdParams& p, const BwdItem& it, int kg) {
+  return (MASK != kMaskNone && p.win_right >= 0) ? kg - it.off - p.win_right : INT_MIN;
+}
+template <int MASK>
+__device__ __forceinline__ int mask_b(const BwdParams& p, const BwdItem& it, int kg) {
+  return MASK == kMaskWindow ? kg - it.off + p.win_left : INT_MAX;
+}
+// Whether some (key, query) pair of keys [k0, k0 + 128) x queries [qs, qs + nq) is hidden.
+template <int MASK>
+__device__ __forceinline__ bool mask_needed(const BwdParams& p, const BwdItem& it, int k0, int qs, int nq) {
+  if (MASK == kMaskNone) return false;
+  return (p.win_right >= 0 && qs < k0 + 127 - it.off - p.win_right) ||
+         (MASK == kMaskWindow && qs + nq - 1 > k0 - it.off + p.win_left);
+}
+
+// No query sees the key block: its dK and dV rows are zero.
+template <int D>
+__device__ void bwd_zero_dkdv(const BwdParams& p, const BwdItem& it, int Hkv, int h_kv, int k0) {
+  const int nk = min(128, it.kv_len - k0);
+  for (int idx = (int)threadIdx.x; idx < nk * (D / 8); idx += (int)blockDim.x) {
+    const int r = idx / (D / 8), c = idx % (D / 8);
+    const size_t grow = ((size_t)it.b_coord * p.n_rows_k + it.kv_start + k0 + r) * Hkv + h_kv;
+    reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dk) + grow * D)[c] = make_uint4(0u, 0u, 0u, 0u);
+    reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dv) + grow * D)[c] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
 // ---------------------------------------------------------------- main
 
-template <int D, bool CAUSAL>
+template <int D, int MASK>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -169,18 +236,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int b = bh / Hkv;
   const int h_kv = bh % Hkv;
   const int jb = (int)blockIdx.y;  // key block; ascending = heaviest first when causal
-  int seq_start = 0, seq_len = p.seq_len, b_coord = b;
-  if (p.cu_seqlens != nullptr) {
-    seq_start = p.cu_seqlens[b];
-    seq_len = p.cu_seqlens[b + 1] - seq_start;
-    b_coord = 0;
-  }
   const int k0 = jb * 128;
-  if (k0 >= seq_len) return;
-  const int n_qblk = (seq_len + 127) / 128;
-  const int i_begin = CAUSAL ? jb : 0;
-  const int n_q = n_qblk - i_begin;       // query blocks per query head
-  const int n_steps = p.kv_group * n_q;   // step n: query head hq(n), query block i_begin + n % n_q
+  const BwdItem it = bwd_item<MASK>(p, b, k0);
+  if (it.bad) {
+    if (threadIdx.x == 0 && p.err != nullptr) atomicCAS(p.err, 0u, FA_DEVERR_BAD_SEQLEN);
+    return;
+  }
+  const int seq_start = it.seq_start, seq_len = it.seq_len, kv_start = it.kv_start, b_coord = it.b_coord;
+  if (k0 >= it.kv_len) return;
+  const int q_begin = it.q_lo;
+  const int n_q = it.q_hi > it.q_lo ? (it.q_hi - it.q_lo + 127) / 128 : 0;  // query blocks per query head
+  if (n_q == 0) {  // uniform for the CTA, before any shared state exists
+    bwd_zero_dkdv<D>(p, it, Hkv, h_kv, k0);
+    return;
+  }
+  const int n_steps = p.kv_group * n_q;   // step n: query head hq(n), rows q_begin + 128 (n % n_q) + [0, 128)
   auto hq_of = [&](int n) { return h_kv * p.kv_group + n / n_q; };
   auto row_base_of = [&](int hq) { return (size_t)(b_coord * p.H + hq) * p.n_rows + seq_start; };  // lse2 / dsum / acc
 
@@ -233,13 +303,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tma_prefetch_desc(&tm_do);
       mbar_arrive_expect_tx(BAR(KV_FULL), 2 * TILE);
       for (int c = 0; c < CH; ++c) {
-        tma_load_4d(sK + c * CHUNK, &tm_k, BAR(KV_FULL), c * 64, seq_start + k0, h_kv, b_coord);
-        tma_load_4d(sV + c * CHUNK, &tm_v, BAR(KV_FULL), c * 64, seq_start + k0, h_kv, b_coord);
+        tma_load_4d(sK + c * CHUNK, &tm_k, BAR(KV_FULL), c * 64, kv_start + k0, h_kv, b_coord);
+        tma_load_4d(sV + c * CHUNK, &tm_v, BAR(KV_FULL), c * 64, kv_start + k0, h_kv, b_coord);
       }
       bool ok = true;
       for (int n = 0; n < n_steps && ok; ++n) {
         const int st = n & 1;
-        const int row = seq_start + (i_begin + n % n_q) * 128;
+        const int row = seq_start + q_begin + (n % n_q) * 128;
         const int hq = hq_of(n);
         if (n >= 2 && !(ok = mbar_wait(BAR(STAGE_EMPTY + st), ((n >> 1) - 1) & 1, w, 21))) break;
         mbar_arrive_expect_tx(BAR(Q_FULL + st), 2 * TILE);
@@ -318,7 +388,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int kw = warp & 3;
     const int kr = kw * 32 + lane;
     const int kg = k0 + kr;
-    const bool row_ok = kg < seq_len;
+    const bool row_ok = kg < it.kv_len;
+    const int ma = mask_a<MASK>(p, it, kg), mb = mask_b<MASK>(p, it, kg);
     const uint32_t lane_off = (uint32_t)(kw * 32) << 16;
     const uint32_t tS = tmem + lane_off, tDP = tmem + lane_off + 128;
     const float sl2 = p.scale_log2;
@@ -329,7 +400,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // this thread's lse2 and D of the next query block, fetched one step ahead
     // (invalid rows: lse2 = +inf, so P = 0)
     auto fetch = [&](int n, float& l2, float& ds) {
-      const int qg = (i_begin + n % n_q) * 128 + kr;
+      const int qg = q_begin + (n % n_q) * 128 + kr;
       const bool qv = n < n_steps && qg < seq_len;
       const size_t rb = n < n_steps ? row_base_of(hq_of(n)) : 0;
       l2 = qv ? p.lse2[rb + qg] : INFINITY;
@@ -338,7 +409,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     float pf_l, pf_d;
     fetch(0, pf_l, pf_d);
     for (int n = 0; n < n_steps; ++n) {
-      const int q0 = (i_begin + n % n_q) * 128;
+      const int q0 = q_begin + (n % n_q) * 128;
       asm volatile("bar.sync 1, 128;" ::: "memory");
       s_lse2[kr] = pf_l;
       s_dsum[kr] = pf_d;
@@ -354,7 +425,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         continue;
       }
       tc_fence_after();
-      const bool diag = CAUSAL && (q0 == k0);
+      const bool masked = mask_needed<MASK>(p, it, k0, q0, 128);
 #pragma unroll 2
       for (int c = 0; c < 8; ++c) {
         uint32_t sr[16], dr[16];
@@ -379,10 +450,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             p0 = 0.f;
             p1 = 0.f;
           }
-          if (diag) {
+          if (masked) {
             const int qg = q0 + 16 * c + e;
-            if (kg > qg) p0 = 0.f;
-            if (kg > qg + 1) p1 = 0.f;
+            if (qg < ma || qg > mb) p0 = 0.f;
+            if (qg + 1 < ma || qg + 1 > mb) p1 = 0.f;
           }
           const float g0 = p0 * scale * (__uint_as_float(dr[e]) - dv[e]);
           const float g1 = p1 * scale * (__uint_as_float(dr[e + 1]) - dv[e + 1]);
@@ -406,7 +477,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = mbar_wait(BAR(DKV_FINAL), 0, w, 29);
       if (__all_sync(0xffffffffu, ok)) {
         tc_fence_after();
-        const size_t grow = ((size_t)b_coord * p.n_rows + seq_start + kg) * Hkv + h_kv;
+        const size_t grow = ((size_t)b_coord * p.n_rows_k + kv_start + kg) * Hkv + h_kv;
         __nv_bfloat16* dv_row = reinterpret_cast<__nv_bfloat16*>(p.dv) + grow * D;
         __nv_bfloat16* dk_row = reinterpret_cast<__nv_bfloat16*>(p.dk) + grow * D;
 #pragma unroll
@@ -437,7 +508,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t tDQ = tmem + ((uint32_t)(qw * 32) << 16) + 128;
     for (int n = 0; n < n_steps; ++n) {
       float4* acc = reinterpret_cast<float4*>(p.dq_acc) + (size_t)(b_coord * p.H + hq_of(n)) * (D / 4) * p.n_rows;
-      const int qg = (i_begin + n % n_q) * 128 + r;
+      const int qg = q_begin + (n % n_q) * 128 + r;
       bool ok = mbar_wait(BAR(DQ_FULL), n & 1, w, 30);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
@@ -447,7 +518,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(BAR(DQ_EMPTY));  // TMEM free for the next dP^T while the adds go out
-      if (qg < seq_len) {
+      if (qg < it.q_hi) {  // rows past q_hi see none of this block's keys: their share is zero
         const size_t row = (size_t)seq_start + qg;
 #pragma unroll
         for (int g = 0; g < D / 4; ++g)
@@ -500,7 +571,7 @@ struct Bwd128Layout {
   static constexpr uint32_t kBytes = kBar + 256 + 1024 + 1024;  // barriers, lse2/D rows, alignment slack
 };
 
-template <bool CAUSAL>
+template <int MASK>
 __global__ void __launch_bounds__(kBwd128Threads, 1)
     fa_bwd_main128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -526,16 +597,20 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
   const int b = bh / Hkv;
   const int h_kv = bh % Hkv;
   const int jb = (int)blockIdx.y;
-  int seq_start = 0, seq_len = p.seq_len, b_coord = b;
-  if (p.cu_seqlens != nullptr) {
-    seq_start = p.cu_seqlens[b];
-    seq_len = p.cu_seqlens[b + 1] - seq_start;
-    b_coord = 0;
-  }
   const int k0 = jb * 128;
-  if (k0 >= seq_len) return;
-  const int q_begin = CAUSAL ? k0 : 0;
-  const int n_q = (seq_len - q_begin + 127) / 128;  // query blocks per query head
+  const BwdItem it = bwd_item<MASK>(p, b, k0);
+  if (it.bad) {
+    if (threadIdx.x == 0 && p.err != nullptr) atomicCAS(p.err, 0u, FA_DEVERR_BAD_SEQLEN);
+    return;
+  }
+  const int seq_start = it.seq_start, seq_len = it.seq_len, kv_start = it.kv_start, b_coord = it.b_coord;
+  if (k0 >= it.kv_len) return;
+  const int q_begin = it.q_lo;
+  const int n_q = it.q_hi > it.q_lo ? (it.q_hi - it.q_lo + 127) / 128 : 0;  // query blocks per query head
+  if (n_q == 0) {  // uniform for the CTA, before any shared state exists
+    bwd_zero_dkdv<D>(p, it, Hkv, h_kv, k0);
+    return;
+  }
   const int n_steps = p.kv_group * n_q;              // step n: query head hq(n), block n % n_q
   auto hq_of = [&](int n) { return h_kv * p.kv_group + n / n_q; };
   auto row_base_of = [&](int hq) { return (size_t)(b_coord * p.H + hq) * p.n_rows + seq_start; };
@@ -588,8 +663,8 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
       tma_prefetch_desc(&tm_do);
       mbar_arrive_expect_tx(BAR(KV_FULL), 2 * L::kTile);
       for (int c = 0; c < 2; ++c) {
-        tma_load_4d(sK + c * CHUNK, &tm_k, BAR(KV_FULL), c * 64, seq_start + k0, h_kv, b_coord);
-        tma_load_4d(sV + c * CHUNK, &tm_v, BAR(KV_FULL), c * 64, seq_start + k0, h_kv, b_coord);
+        tma_load_4d(sK + c * CHUNK, &tm_k, BAR(KV_FULL), c * 64, kv_start + k0, h_kv, b_coord);
+        tma_load_4d(sV + c * CHUNK, &tm_v, BAR(KV_FULL), c * 64, kv_start + k0, h_kv, b_coord);
       }
       bool ok = true;
       for (int n = 0; n < n_steps && ok; ++n) {
@@ -686,7 +761,8 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
     const int kw = warp & 3;
     const int kr = kw * 32 + lane;
     const int kg = k0 + kr;
-    const bool row_ok = kg < seq_len;
+    const bool row_ok = kg < it.kv_len;
+    const int ma = mask_a<MASK>(p, it, kg), mb = mask_b<MASK>(p, it, kg);
     const uint32_t lane_off = (uint32_t)(kw * 32) << 16;
     const int swz = kr & 7;
     float* my_lse2 = s_lse2 + 64 * g;
@@ -722,8 +798,8 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
         continue;
       }
       tc_fence_after();
-      const bool diag = CAUSAL && (qs < k0 + 127);
-      const bool tail_rows = k0 + 128 > seq_len;  // only the last key block has rows past the end
+      const bool masked = mask_needed<MASK>(p, it, k0, qs, 64);
+      const bool tail_rows = k0 + 128 > it.kv_len;  // only the last key block has rows past the end
       const float sl2 = p.scale_log2, scale = p.scale;
       uint8_t* ds_row = sbase + L::kDS + g * CHUNK + kr * 128;
 #pragma unroll 1
@@ -755,10 +831,11 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
             pv[4 * e4 + 2] = ex2_sfu(fmaf(__uint_as_float(sr[4 * e4 + 2]), sl2, nl.z));
             pv[4 * e4 + 3] = ex2_sfu(fmaf(__uint_as_float(sr[4 * e4 + 3]), sl2, nl.w));
           }
-          if (diag || (tail_rows && !row_ok)) {  // masks in a separate, warp-uniform pass
+          if (masked || (tail_rows && !row_ok)) {  // masks in a separate, warp-uniform pass
+            const int q16 = qs + 32 * r + 16 * hh;
 #pragma unroll
             for (int e = 0; e < 16; ++e)
-              if (!row_ok || (diag && kg > qs + 32 * r + 16 * hh + e)) pv[e] = 0.f;
+              if (!row_ok || (masked && (q16 + e < ma || q16 + e > mb))) pv[e] = 0.f;
           }
           // dS = P * (scale * dP - scale * D)
           uint32_t pp[8], dd[8];
@@ -793,7 +870,7 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
       ok = mbar_wait(BAR(DKV_FINAL), 0, w, 59);
       if (__all_sync(0xffffffffu, ok)) {
         tc_fence_after();
-        const size_t grow = ((size_t)b_coord * p.n_rows + seq_start + kg) * Hkv + h_kv;
+        const size_t grow = ((size_t)b_coord * p.n_rows_k + kv_start + kg) * Hkv + h_kv;
         const uint32_t src = tmem + lane_off + (g ? 384u : 256u);
         __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(g ? p.dk : p.dv) + grow * D;
 #pragma unroll
@@ -823,7 +900,7 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
     for (int n = 0; n < n_steps; ++n) {
       float* acc = p.dq_acc + row_base_of(hq_of(n)) * D + dr;  // [B*H][rows][d]: a warp's lanes cover 128 bytes
       const int q0 = q_begin + (n % n_q) * 128 + 64 * half;
-      const int nq = min(64, seq_len - q0);
+      const int nq = min(64, it.q_hi - q0);  // rows past q_hi see none of this block's keys
       bool ok = mbar_wait(BAR(DQ_FULL), n & 1, w, 60);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
@@ -848,7 +925,16 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
   }
 }
 
-template <int D, bool CAUSAL>
+// d = 128 runs the overlapped kernel, d = 64 the serial one (only the chosen one is instantiated).
+template <int D, int MASK>
+static auto main_kernel_for() {
+  if constexpr (D == 128)
+    return fa_bwd_main128_kernel<MASK>;
+  else
+    return fa_bwd_main_kernel<D, MASK>;
+}
+
+template <int D, int MASK>
 static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream) {
   const long long rows = (long long)p.B_tensor * p.H * p.n_rows;
@@ -858,7 +944,7 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
-  auto kern = D == 128 ? fa_bwd_main128_kernel<CAUSAL> : fa_bwd_main_kernel<D, CAUSAL>;
+  auto kern = main_kernel_for<D, MASK>();
   constexpr uint32_t smem = D == 128 ? Bwd128Layout::kBytes : BwdLayout<D>::kBytes;
   static bool configured = false;
   if (!configured) {
@@ -880,11 +966,16 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
 }
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                       const BwdParams& p, int D, bool causal, cudaStream_t stream) {
-  if (D == 64) return causal ? launch_bwd_t<64, true>(tq, tk, tv, tdo, p, stream)
-                             : launch_bwd_t<64, false>(tq, tk, tv, tdo, p, stream);
-  if (D == 128) return causal ? launch_bwd_t<128, true>(tq, tk, tv, tdo, p, stream)
-                              : launch_bwd_t<128, false>(tq, tk, tv, tdo, p, stream);
+                       const BwdParams& p, int D, int mask, cudaStream_t stream) {
+#define FA_BWD_CASE(DD, MM) \
+  if (D == DD && mask == MM) return launch_bwd_t<DD, MM>(tq, tk, tv, tdo, p, stream);
+  FA_BWD_CASE(64, kMaskNone)
+  FA_BWD_CASE(64, kMaskRight)
+  FA_BWD_CASE(64, kMaskWindow)
+  FA_BWD_CASE(128, kMaskNone)
+  FA_BWD_CASE(128, kMaskRight)
+  FA_BWD_CASE(128, kMaskWindow)
+#undef FA_BWD_CASE
   return cudaErrorInvalidValue;
 }
 

@@ -14,6 +14,12 @@
 // The conditional rescale ("And on Blackwell") keeps a stale reference
 // maximum until the true maximum has grown by more than 2^tau; l and O~ share
 // the reference, so the final division cancels it and the result is exact.
+// Masks (causal, sliding window) are bottom-right aligned: query i of a
+// sequence with Nq queries and Nk keys sits at key position i + Nk - Nq and
+// sees keys [i + Nk - Nq - w_left, i + Nk - Nq + w_right] ("efficient-attention/
+// flash-2-3", "Using it, the real way": FlashAttention kernels handle causal masks and sliding windows
+// natively; tiles outside every row's window are never visited, the
+// block-sparse skipping that FlexAttention's block mask performs).
 // Part of the exponentials may be evaluated on the FMA pipe as
 // 2^floor(x) * p3(x - floor(x)) with a cubic fitted in fit_exp2_poly.py.
 //
@@ -66,11 +72,13 @@ constexpr int kHeadGroup = 8;  // heads whose CTAs are scheduled together
 
 }  // namespace
 
-template <int D, bool CAUSAL, bool POLY>
+template <int D, int MASK, bool POLY>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using L = FwdLayout<D>;
+  constexpr bool MASKED = MASK != kMaskNone;
+  constexpr bool LEFT = MASK == kMaskWindow;  // rows' keys may start after key 0
   constexpr int NS = L::kStages;
   constexpr int CH = D / 64;
   constexpr uint32_t TILE = L::kTile;
@@ -93,29 +101,46 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int h = bh % p.H;
   const int h_kv = h / p.kv_group;  // grouped-query attention: K/V head shared by kv_group query heads
   const int pair = p.num_pairs - 1 - (int)blockIdx.y;  // heaviest causal pairs first
-  int seq_start = 0, seq_len = p.seq_len, b_coord = b;
+  int seq_start = 0, seq_len = p.seq_len, kv_start = 0, kv_len = p.seq_len_k, b_coord = b;
   if (p.cu_seqlens != nullptr) {
     seq_start = p.cu_seqlens[b];
     seq_len = p.cu_seqlens[b + 1] - seq_start;
+    kv_start = p.cu_seqlens_k[b];
+    kv_len = p.cu_seqlens_k[b + 1] - kv_start;
     b_coord = 0;
+    if (seq_start < 0 || seq_len < 0 || seq_start > p.n_rows - seq_len || kv_start < 0 || kv_len < 0 ||
+        kv_start > p.n_rows_k - kv_len) {  // offsets outside the tensors: report, touch nothing
+      if (threadIdx.x == 0 && p.err != nullptr) atomicCAS(p.err, 0u, FA_DEVERR_BAD_SEQLEN);
+      return;
+    }
   }
   const int q0 = pair * 256;
   if (q0 >= seq_len) return;  // uniform for the CTA, before any shared state exists
 
-  const int n_kv_all = (seq_len + 127) / 128;
-  int nkv[2];
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
+  // Key tiles each query tile t visits: [jlo_t, jhi_t).  A tile's rows see
+  // keys [key_lo(first row), key_hi(last row)) between them (both bounds grow
+  // with the row), so the tiles outside that range are skipped entirely.
+  auto tile_range = [&](int t, int& lo_t, int& hi_t) {
     const int r0 = q0 + 128 * t;
-    if (r0 >= seq_len) {
-      nkv[t] = 0;
-    } else if (CAUSAL) {
-      nkv[t] = min(n_kv_all, min(r0 + 127, seq_len - 1) / 128 + 1);
-    } else {
-      nkv[t] = n_kv_all;
+    lo_t = hi_t = 0;
+    if (r0 < seq_len) {
+      const int r1 = min(r0 + 127, seq_len - 1);
+      const int lo = LEFT ? mask_key_lo(r0, seq_len, kv_len, p.win_left) : 0;
+      const int hi = MASKED ? mask_key_hi(r1, seq_len, kv_len, p.win_right) : kv_len;
+      if (hi > lo) {
+        lo_t = lo / 128;
+        hi_t = (hi + 127) / 128;
+      }
     }
-  }
-  const int nkv_max = max(nkv[0], nkv[1]);
+  };
+  int jlo0, jhi0, jlo1, jhi1;
+  tile_range(0, jlo0, jhi0);
+  tile_range(1, jlo1, jhi1);
+  // The producer streams the union of the two ranges; it is contiguous, since
+  // tile 1 starts no later than tile 0 ends (window_left + window_right >= 0).
+  const bool live0 = jhi0 > jlo0, live1 = jhi1 > jlo1;
+  const int jmin = live0 ? jlo0 : jlo1;
+  const int jmax = live1 ? jhi1 : jhi0;
 
   // ---------------------------------------------------------------- barriers
   enum { Q_FULL = 0, KV_FULL = 1, KV_EMPTY = 1 + NS, S_FULL = 1 + 2 * NS, P_FULL = S_FULL + 2, O_FINAL = P_FULL + 2,
@@ -164,9 +189,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < CH; ++c)
           tma_load_4d(q_s + t * TILE + c * CHUNK, &tm_q, BAR(Q_FULL), c * 64, seq_start + q0 + 128 * t, h, b_coord);
       bool ok = true;
-      for (int j = 0; j < nkv_max && ok; ++j) {
+      for (int j = jmin; j < jmax && ok; ++j) {
         for (int which = 0; which < 2; ++which) {
-          const int u = 2 * j + which;
+          const int u = 2 * (j - jmin) + which;
           const int slot = u % NS;
           if (u >= NS && !mbar_wait(BAR(KV_EMPTY + slot), ((u / NS) - 1) & 1, w, 1)) {
             ok = false;
@@ -175,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(BAR(KV_FULL + slot), TILE);
           const CUtensorMap* m = which ? &tm_v : &tm_k;
           for (int c = 0; c < CH; ++c)
-            tma_load_4d(kv_s + slot * TILE + c * CHUNK, m, BAR(KV_FULL + slot), c * 64, seq_start + 128 * j, h_kv,
+            tma_load_4d(kv_s + slot * TILE + c * CHUNK, m, BAR(KV_FULL + slot), c * 64, kv_start + 128 * j, h_kv,
                         b_coord);
         }
       }
@@ -216,46 +241,48 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       ok = mbar_wait(BAR(Q_FULL), 0, w, 2);
       tc_fence_after();
-      for (int j = 0; j < nkv_max && ok; ++j) {
-        const int uk = 2 * j, sk = uk % NS;
+      // Ring position u of key tile j is 2 (j - jmin) (K) and 2 (j - jmin) + 1 (V);
+      // tile t's S / P barriers complete once per visited key tile, phase j - jlo_t.
+      for (int j = jmin; j < jmax && ok; ++j) {
+        const int uk = 2 * (j - jmin), sk = uk % NS;
         if (!(ok = mbar_wait(BAR(KV_FULL + sk), (uk / NS) & 1, w, 3))) break;
         tc_fence_after();
-        if (j < nkv[0]) {
+        if (j >= jlo0 && j < jhi0) {
           issue_S(0, sk);
           mma_commit(BAR(S_FULL + 0));
         }
-        if (j >= 1) {
-          const int sv = (2 * (j - 1) + 1) % NS;
-          if (j - 1 < nkv[1]) {
-            if (!(ok = mbar_wait(BAR(P_FULL + 1), (j - 1) & 1, w, 4))) break;
+        if (j > jmin) {
+          const int sv = (uk - 1) % NS;
+          if (j - 1 >= jlo1 && j - 1 < jhi1) {
+            if (!(ok = mbar_wait(BAR(P_FULL + 1), (j - 1 - jlo1) & 1, w, 4))) break;
             tc_fence_after();
-            issue_PV(1, sv, j - 1 > 0);
-            if (j - 1 == nkv[1] - 1) mma_commit(BAR(O_FINAL + 1));
+            issue_PV(1, sv, j - 1 > jlo1);
+            if (j - 1 == jhi1 - 1) mma_commit(BAR(O_FINAL + 1));
           }
           mma_commit(BAR(KV_EMPTY + sv));
         }
-        if (j < nkv[1]) {
+        if (j >= jlo1 && j < jhi1) {
           issue_S(1, sk);
           mma_commit(BAR(S_FULL + 1));
         }
         mma_commit(BAR(KV_EMPTY + sk));
-        const int uv = 2 * j + 1, sv = uv % NS;
+        const int uv = uk + 1, sv = uv % NS;
         if (!(ok = mbar_wait(BAR(KV_FULL + sv), (uv / NS) & 1, w, 5))) break;
         tc_fence_after();
-        if (j < nkv[0]) {
-          if (!(ok = mbar_wait(BAR(P_FULL + 0), j & 1, w, 6))) break;
+        if (j >= jlo0 && j < jhi0) {
+          if (!(ok = mbar_wait(BAR(P_FULL + 0), (j - jlo0) & 1, w, 6))) break;
           tc_fence_after();
-          issue_PV(0, sv, j > 0);
-          if (j == nkv[0] - 1) mma_commit(BAR(O_FINAL + 0));
+          issue_PV(0, sv, j > jlo0);
+          if (j == jhi0 - 1) mma_commit(BAR(O_FINAL + 0));
         }
       }
-      if (ok && nkv_max >= 1) {
-        const int j = nkv_max;
-        const int sv = (2 * (j - 1) + 1) % NS;
-        if (j - 1 < nkv[1]) {
-          if ((ok = mbar_wait(BAR(P_FULL + 1), (j - 1) & 1, w, 4))) {
+      if (ok && jmax > jmin) {
+        const int j = jmax;
+        const int sv = (2 * (j - 1 - jmin) + 1) % NS;
+        if (j - 1 >= jlo1 && j - 1 < jhi1) {
+          if ((ok = mbar_wait(BAR(P_FULL + 1), (j - 1 - jlo1) & 1, w, 4))) {
             tc_fence_after();
-            issue_PV(1, sv, j - 1 > 0);
+            issue_PV(1, sv, j - 1 > jlo1);
             mma_commit(BAR(O_FINAL + 1));
           }
         }
@@ -282,9 +309,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_ref = -INFINITY;
     float l = 0.f;
     bool ok = true;
+    // keys this row sees: [key_lo, key_hi)
+    const int key_lo = LEFT ? mask_key_lo(row, seq_len, kv_len, p.win_left) : 0;
+    const int key_hi = MASKED ? mask_key_hi(row, seq_len, kv_len, p.win_right) : kv_len;
+    const int jlo = t ? jlo1 : jlo0, jhi = t ? jhi1 : jhi0;
 
-    for (int j = 0; j < nkv[t]; ++j) {
-      ok = mbar_wait(BAR(S_FULL + t), j & 1, w, 7);
+    for (int j = jlo; j < jhi; ++j) {
+      ok = mbar_wait(BAR(S_FULL + t), (j - jlo) & 1, w, 7);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
@@ -299,11 +330,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < 128; ++i) x[i] = __uint_as_float(sr[i / 32][i % 32]);
 
       const int kv0 = 128 * j;
-      const int lim = CAUSAL ? min(row + 1, seq_len) : seq_len;  // visible keys are < lim
-      if (kv0 + 128 > lim) {
+      if ((LEFT && kv0 < key_lo) || kv0 + 128 > key_hi) {
 #pragma unroll
         for (int i = 0; i < 128; ++i)
-          if (kv0 + i >= lim) x[i] = -INFINITY;
+          if ((LEFT && kv0 + i < key_lo) || kv0 + i >= key_hi) x[i] = -INFINITY;
       }
       // row maximum: eight short chains of 3-input maxima, then a small tree
       float mg[8];
@@ -352,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       f2_unpack(acc[3], s6, s7);
       l = l * alpha + (((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7)));
 
-      if (j > 0 && __any_sync(0xffffffffu, resc)) {
+      if (j > jlo && __any_sync(0xffffffffu, resc)) {
         // rows whose reference moved: O~ *= alpha (alpha = 1 for the others)
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -371,14 +401,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ------------------------------------------------------------ epilogue
-    if (ok && nkv[t] > 0) {
+    const bool row_ok = row < seq_len;
+    __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) +
+                          (((size_t)b_coord * p.n_rows + seq_start + row) * p.H + h) * D;
+    float* lse_out = p.lse + ((size_t)b_coord * p.H + h) * p.n_rows + seq_start + row;
+    if (jhi <= jlo) {
+      // no key tile visible to any row of this tile: O = 0, lse = -inf
+      if (row_ok) {
+        uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+        *lse_out = -INFINITY;
+      }
+    } else if (ok) {
       ok = mbar_wait(BAR(O_FINAL + t), 0, w, 8);
       if (__all_sync(0xffffffffu, ok)) {
         tc_fence_after();
-        const bool row_ok = row < seq_len;
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
-        __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) +
-                              (((size_t)b_coord * p.n_rows + seq_start + row) * p.H + h) * D;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t ov[32];
@@ -394,10 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
           }
         }
-        if (row_ok) {
-          const float lse = l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-          p.lse[((size_t)b_coord * p.H + h) * p.n_rows + seq_start + row] = lse;
-        }
+        if (row_ok) *lse_out = l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
       }
     }
   }
@@ -411,10 +447,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool POLY>
+template <int D, int MASK, bool POLY>
 static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const FwdParams& p, int grid_x, cudaStream_t stream) {
-  auto kern = fa_fwd_kernel<D, CAUSAL, POLY>;
+  auto kern = fa_fwd_kernel<D, MASK, POLY>;
   constexpr uint32_t smem = FwdLayout<D>::kBytes;
   static bool configured = false;
   if (!configured) {
@@ -429,17 +465,19 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
 }
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
-                       int D, bool causal, bool poly, int grid_x, cudaStream_t stream) {
-#define FA_FWD_CASE(DD, CC, PP) \
-  if (D == DD && causal == CC && poly == PP) return launch_fwd_t<DD, CC, PP>(tq, tk, tv, p, grid_x, stream);
-  FA_FWD_CASE(64, false, false)
-  FA_FWD_CASE(64, false, true)
-  FA_FWD_CASE(64, true, false)
-  FA_FWD_CASE(64, true, true)
-  FA_FWD_CASE(128, false, false)
-  FA_FWD_CASE(128, false, true)
-  FA_FWD_CASE(128, true, false)
-  FA_FWD_CASE(128, true, true)
+                       int D, int mask, bool poly, int grid_x, cudaStream_t stream) {
+#define FA_FWD_CASE(DD, MM, PP) \
+  if (D == DD && mask == MM && poly == PP) return launch_fwd_t<DD, MM, PP>(tq, tk, tv, p, grid_x, stream);
+#define FA_FWD_CASES(DD)         \
+  FA_FWD_CASE(DD, kMaskNone, false)   \
+  FA_FWD_CASE(DD, kMaskNone, true)    \
+  FA_FWD_CASE(DD, kMaskRight, false)  \
+  FA_FWD_CASE(DD, kMaskRight, true)   \
+  FA_FWD_CASE(DD, kMaskWindow, false) \
+  FA_FWD_CASE(DD, kMaskWindow, true)
+  FA_FWD_CASES(64)
+  FA_FWD_CASES(128)
+#undef FA_FWD_CASES
 #undef FA_FWD_CASE
   return cudaErrorInvalidValue;
 }

@@ -12,12 +12,17 @@ namespace fa {
 struct FwdParams {
   void* o;                   // bf16 output
   float* lse;                // fp32 log-sum-exp
-  const int* cu_seqlens;     // packed batch offsets (device) or nullptr for a dense batch
+  const int* cu_seqlens;     // packed query offsets (device) or nullptr for a dense batch
+  const int* cu_seqlens_k;   // packed key offsets (device); set exactly when cu_seqlens is
   int H;                     // query heads
   int kv_group;              // query heads per K/V head (grouped-query attention; 1 = one K/V head per query head)
   int bh_total;              // (batch or sequences) * H
-  int n_rows;                // rows along the sequence axis of the tensors (N, or total tokens)
-  int seq_len;               // dense: N
+  int n_rows;                // rows along the sequence axis of Q and O (Nq, or total query tokens)
+  int n_rows_k;              // rows along the sequence axis of K and V (Nk, or total key tokens)
+  int seq_len;               // dense: Nq
+  int seq_len_k;             // dense: Nk
+  int win_left;              // mask (used by the masked kernels): query i sees keys
+  int win_right;             //   [i + Nk - Nq - win_left, i + Nk - Nq + win_right]; -1 = unbounded side
   int num_pairs;             // grid.y: pairs of 128-row query tiles per (sequence, head)
   float scale_log2;          // scale * log2(e)
   float tau;                 // lazy-rescale threshold, log2 units
@@ -35,13 +40,18 @@ struct BwdParams {
   void* dq;
   void* dk;
   void* dv;
-  const int* cu_seqlens;     // packed batch offsets (device) or nullptr
+  const int* cu_seqlens;     // packed query offsets (device) or nullptr
+  const int* cu_seqlens_k;   // packed key offsets (device); set exactly when cu_seqlens is
   int B;                     // dense batch, or number of sequences
   int B_tensor;              // leading extent of the tensors: B (dense) or 1 (packed)
   int H;                     // query heads
   int kv_group;              // query heads per K/V head (1 = one K/V head per query head)
-  int n_rows;                // rows along the sequence axis of the tensors
-  int seq_len;               // dense: N
+  int n_rows;                // rows along the sequence axis of Q, O, dO, dQ
+  int n_rows_k;              // rows along the sequence axis of K, V, dK, dV
+  int seq_len;               // dense: Nq
+  int seq_len_k;             // dense: Nk
+  int win_left;              // mask, as in FwdParams
+  int win_right;
   int num_kblocks;           // grid.y of the main kernel
   float scale;
   float scale_log2;
@@ -53,11 +63,33 @@ struct BwdParams {
 // box and 128-byte swizzle.  Returns false when the driver refuses it.
 bool make_tmap_bhnd(CUtensorMap* m, const void* ptr, int D, int n_rows, int H, int B, int box_rows = 128);
 
+// Mask kinds the kernels are specialised for: none; a right bound only
+// (causal-like, every row's keys start at 0); any other window.
+enum MaskKind { kMaskNone = 0, kMaskRight = 1, kMaskWindow = 2 };
+inline int mask_kind(int win_left, int win_right) {
+  return win_left >= 0 ? kMaskWindow : (win_right >= 0 ? kMaskRight : kMaskNone);
+}
+
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
-                       int D, bool causal, bool poly, int grid_x, cudaStream_t stream);
+                       int D, int mask, bool poly, int grid_x, cudaStream_t stream);
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const BwdParams& p, int D, bool causal, cudaStream_t stream);
+                       const CUtensorMap& tdo, const BwdParams& p, int D, int mask, cudaStream_t stream);
+
+// Keys visible to query row i of a sequence with nq queries and nk keys:
+// [key_lo, key_hi).  Bottom-right aligned: query i sits at key position
+// i + nk - nq; win_left / win_right < 0 leave that side unbounded.  Causal is
+// win_left = -1, win_right = 0.
+__host__ __device__ __forceinline__ int mask_key_lo(int i, int nq, int nk, int win_left) {
+  if (win_left < 0) return 0;
+  const long long lo = (long long)i + nk - nq - win_left;
+  return lo < 0 ? 0 : (lo > nk ? nk : (int)lo);
+}
+__host__ __device__ __forceinline__ int mask_key_hi(int i, int nq, int nk, int win_right) {
+  if (win_right < 0) return nk;
+  const long long hi = (long long)i + nk - nq + win_right + 1;
+  return hi < 0 ? 0 : (hi > nk ? nk : (int)hi);
+}
 
 struct DecodeParams {
   const void* q;             // [B, 1, H, d] bf16

@@ -260,3 +260,114 @@ def decode_gqa(q, k_cache, v_cache, num_splits: int = 0, scale: Optional[float] 
                              _ptr(ws), scale, _stream(stream))
     _lib.check(st, "fa_decode_gqa")
     return o, l
+
+
+# ---------------------------------------------------------------- masks: causal / sliding window, Nq != Nk
+
+def _window(causal: bool, window: Optional[Tuple[int, int]]):
+    """(window_left, window_right) of the C ABI; ``causal`` alone is (-1, 0)."""
+    if window is None:
+        return (-1, 0) if causal else (-1, -1)
+    wl, wr = int(window[0]), int(window[1])
+    if causal:
+        wr = 0 if wr < 0 else min(wr, 0)
+    return wl, wr
+
+
+def fwd_masked(q, k, v, causal: bool = False, window: Optional[Tuple[int, int]] = None,
+               scale: Optional[float] = None, stream=None):
+    """q [B, Nq, Hq, d]; k, v [B, Nk, Hkv, d].  Bottom-right aligned mask:
+    query i sees keys i + Nk - Nq - window[0] .. i + Nk - Nq + window[1]
+    (-1 = open side; ``causal`` caps window[1] at 0).
+    Returns (o [B, Nq, Hq, d], lse [B, Hq, Nq])."""
+    _check_bf16("q", q)
+    B, Nq, Hq, d = q.shape
+    _check_bf16("k", k)
+    Nk, Hkv = k.shape[1], k.shape[2]
+    if tuple(k.shape) != (B, Nk, Hkv, d):
+        raise ValueError("k must be [B, Nk, Hkv, d]")
+    _check_bf16("v", v, k.shape)
+    wl, wr = _window(causal, window)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q)
+    l = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    st = lib().fa_fwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, Hq, Hkv, Nq, Nk, d, wl, wr, scale,
+                             _stream(stream))
+    _lib.check(st, "fa_fwd_masked")
+    return o, l
+
+
+def bwd_masked(q, k, v, o, lse, dout, causal: bool = False, window: Optional[Tuple[int, int]] = None,
+               scale: Optional[float] = None, stream=None):
+    """Gradients of fwd_masked: (dq [B, Nq, Hq, d], dk, dv [B, Nk, Hkv, d])."""
+    for name, t in (("q", q), ("o", o), ("dout", dout)):
+        _check_bf16(name, t, q.shape)
+    B, Nq, Hq, d = q.shape
+    _check_bf16("k", k)
+    Nk, Hkv = k.shape[1], k.shape[2]
+    _check_bf16("v", v, k.shape)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, Nq) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous fp32 [B, Hq, Nq]")
+    wl, wr = _window(causal, window)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    nbytes = lib().fa_bwd_workspace_bytes(B, Hq, Nq, d)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    st = lib().fa_bwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                             _ptr(dv), _ptr(ws), B, Hq, Hkv, Nq, Nk, d, wl, wr, scale, _stream(stream))
+    _lib.check(st, "fa_bwd_masked")
+    return dq, dk, dv
+
+
+def fwd_masked_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
+                      causal: bool = False, window: Optional[Tuple[int, int]] = None,
+                      scale: Optional[float] = None, stream=None):
+    """Packed fwd_masked: q [total_q, Hq, d]; k, v [total_k, Hkv, d]; int32
+    offsets on the device.  Returns (o [total_q, Hq, d], lse [Hq, total_q])."""
+    _check_bf16("q", q)
+    total_q, Hq, d = q.shape
+    _check_bf16("k", k)
+    total_k, Hkv = k.shape[0], k.shape[1]
+    if tuple(k.shape) != (total_k, Hkv, d):
+        raise ValueError("k must be [total_k, Hkv, d]")
+    _check_bf16("v", v, k.shape)
+    _check_cu(cu_seqlens_q, q)
+    _check_cu(cu_seqlens_k, q)
+    if cu_seqlens_q.numel() != cu_seqlens_k.numel():
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must have the same length")
+    wl, wr = _window(causal, window)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q)
+    l = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
+    st = lib().fa_fwd_masked_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), _ptr(cu_seqlens_q),
+                                    _ptr(cu_seqlens_k), cu_seqlens_q.numel() - 1, int(max_seqlen_q),
+                                    int(max_seqlen_k), total_q, total_k, Hq, Hkv, d, wl, wr, scale, _stream(stream))
+    _lib.check(st, "fa_fwd_masked_varlen")
+    return o, l
+
+
+def bwd_masked_varlen(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
+                      causal: bool = False, window: Optional[Tuple[int, int]] = None,
+                      scale: Optional[float] = None, stream=None):
+    """Gradients of fwd_masked_varlen: (dq [total_q, Hq, d], dk, dv [total_k, Hkv, d])."""
+    for name, t in (("q", q), ("o", o), ("dout", dout)):
+        _check_bf16(name, t, q.shape)
+    total_q, Hq, d = q.shape
+    _check_bf16("k", k)
+    total_k, Hkv = k.shape[0], k.shape[1]
+    _check_bf16("v", v, k.shape)
+    _check_cu(cu_seqlens_q, q)
+    _check_cu(cu_seqlens_k, q)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (Hq, total_q) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous fp32 [Hq, total_q]")
+    wl, wr = _window(causal, window)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    nbytes = lib().fa_bwd_varlen_workspace_bytes(total_q, Hq, d)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    st = lib().fa_bwd_masked_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                                    _ptr(dv), _ptr(ws), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+                                    cu_seqlens_q.numel() - 1, int(max_seqlen_q), int(max_seqlen_k), total_q, total_k,
+                                    Hq, Hkv, d, wl, wr, scale, _stream(stream))
+    _lib.check(st, "fa_bwd_masked_varlen")
+    return dq, dk, dv

@@ -146,6 +146,68 @@ fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void*
                         fa_stream_t stream);
 
 /*
+ * Masked attention: causal or sliding-window masks with their own query and
+ * key lengths, as used by chunked prefill against a longer cache
+ * ("efficient-attention/flash-2-3", section "Using it, the real way":
+ * FlashAttention kernels support causal masks, sliding windows
+ * and variable lengths natively; PyTorch's is_causal is aligned to the top
+ * left and is wrong for chunked prefill, where the bottom-right alignment of
+ * the flash-attn package is the one wanted).
+ *
+ * Mask, bottom-right aligned: query i of a sequence with Nq queries and Nk keys
+ * sits at key position i + Nk - Nq and sees the keys j with
+ *     i + Nk - Nq - window_left <= j <= i + Nk - Nq + window_right,
+ * a bound of -1 leaving its side open.  (-1, -1) is no mask, (-1, 0) causal,
+ * (w, 0) causal with a window of w + 1 keys.  Key tiles that no row of a
+ * 128-row query tile sees are never loaded ("create_block_mask ... skips
+ * them": block-sparse attention).  A query row that sees no key gets O = 0 and
+ * lse = -inf.  Nk = 0 is allowed: every row is such a row.
+ *   q, o   : [B, Nq, Hq, d] bf16       k, v : [B, Nk, Hkv, d] bf16 (Hkv divides Hq)
+ *   lse    : [B, Hq, Nq] fp32, natural log, written
+ *   window_left, window_right : >= -1; values past the sequence mean no bound
+ * Returns FA_ERR_INVALID_ARG for a bound below -1; otherwise as fa_fwd_gqa.
+ */
+fa_status fa_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                        int Nq, int Nk, int d, int window_left, int window_right, float scale, fa_stream_t stream);
+
+/*
+ * fa_fwd_masked on a packed batch: sequence b owns query rows
+ * cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and key rows cu_seqlens_k[b] ..
+ * cu_seqlens_k[b+1]-1, and the mask aligns the two at the bottom right.
+ *   q, o : [total_q, Hq, d];  k, v : [total_k, Hkv, d];  lse : [Hq, total_q]
+ *   cu_seqlens_q, cu_seqlens_k : int32 [num_seqs + 1], DEVICE memory, as in
+ *                fa_fwd_varlen; offsets outside the tensors are reported by
+ *                fa_device_error (FA_ERR_INVALID_ARG) and nothing is written
+ *                for that sequence
+ *   max_seqlen_q, max_seqlen_k : upper bounds of the sequences' lengths
+ */
+fa_status fa_fwd_masked_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                               const int* cu_seqlens_q, const int* cu_seqlens_k, int num_seqs, int max_seqlen_q,
+                               int max_seqlen_k, int total_q, int total_k, int Hq, int Hkv, int d, int window_left,
+                               int window_right, float scale, fa_stream_t stream);
+
+/*
+ * Backward pass of fa_fwd_masked (Nq, Nk >= 1).  dK, dV of keys that no query
+ * sees are zero; dK, dV sum over the query heads of each K/V head's group.
+ *   q, o, dout, dq : [B, Nq, Hq, d];  k, v, dk, dv : [B, Nk, Hkv, d];  lse [B, Hq, Nq]
+ *   workspace      : fa_bwd_workspace_bytes(B, Hq, Nq, d) bytes
+ */
+fa_status fa_bwd_masked(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                        const void* dout, void* dq, void* dk, void* dv, void* workspace, int B, int Hq, int Hkv,
+                        int Nq, int Nk, int d, int window_left, int window_right, float scale, fa_stream_t stream);
+
+/*
+ * Backward pass of fa_fwd_masked_varlen (total_q, total_k >= 1); tensors in the
+ * packed layout of the forward.
+ *   workspace : fa_bwd_varlen_workspace_bytes(total_q, Hq, d) bytes
+ */
+fa_status fa_bwd_masked_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                               const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                               const int* cu_seqlens_q, const int* cu_seqlens_k, int num_seqs, int max_seqlen_q,
+                               int max_seqlen_k, int total_q, int total_k, int Hq, int Hkv, int d, int window_left,
+                               int window_right, float scale, fa_stream_t stream);
+
+/*
  * Size of the built-in scratch of fa_bwd_noalloc: 32 MiB of device memory,
  * compiled into the library and held by every GPU that loads it until the
  * process exits.

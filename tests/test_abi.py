@@ -82,3 +82,22 @@ def test_options(lib):
     assert lib.fa_set_option(_lib.FA_OPT_RESCALE_TAU, 8.0) == _lib.FA_OK
     assert lib.fa_set_option(99, 1.0) == _lib.FA_ERR_INVALID_ARG
     assert lib.fa_set_option(_lib.FA_OPT_WAIT_TIMEOUT_MS, 0.0) == _lib.FA_ERR_INVALID_ARG
+
+
+def test_masked_validation(lib):
+    def f(wl=-1, wr=0, d=128, Nq=16, Nk=32, Hq=4, Hkv=2, q=A):
+        return lib.fa_fwd_masked(q, A, A, A, A, 1, Hq, Hkv, Nq, Nk, d, wl, wr, 0.1, P(0))
+    assert f(wl=-2) == _lib.FA_ERR_INVALID_ARG
+    assert f(wr=-7) == _lib.FA_ERR_INVALID_ARG
+    assert f(d=96) == _lib.FA_ERR_UNSUPPORTED
+    assert f(Hkv=3) == _lib.FA_ERR_INVALID_ARG
+    assert f(q=MIS) == _lib.FA_ERR_MISALIGNED
+    assert f(Nq=0) == _lib.FA_OK
+    b = lib.fa_bwd_masked
+    assert b(A, A, A, A, A, A, A, A, A, A, 1, 4, 2, 16, 32, 128, -3, 0, 0.1, P(0)) == _lib.FA_ERR_INVALID_ARG
+    assert b(A, A, A, A, A, A, A, A, A, A, 1, 4, 2, 0, 32, 128, -1, 0, 0.1, P(0)) == _lib.FA_ERR_INVALID_ARG
+    fv = lib.fa_fwd_masked_varlen
+    assert fv(A, A, A, A, A, P(0), A, 2, 8, 8, 16, 16, 2, 2, 128, -1, 0, 0.1, P(0)) == _lib.FA_ERR_INVALID_ARG
+    assert fv(A, A, A, A, A, A, MIS, 2, 8, 8, 16, 16, 2, 2, 128, -1, 0, 0.1, P(0)) == _lib.FA_ERR_MISALIGNED
+    assert fv(A, A, A, A, A, A, A, 2, 8, 0, 16, 16, 2, 2, 128, -1, 0, 0.1, P(0)) == _lib.FA_ERR_INVALID_ARG
+    assert fv(A, A, A, A, A, A, A, 2, 8, 8, 0, 16, 2, 2, 128, -1, 0, 0.1, P(0)) == _lib.FA_OK
