@@ -253,11 +253,11 @@ def run_ours(args):
     # roofline of the dominant kernel (largest share of the step)
     if have_bwd and bwd_mean > fwd_mean:
         ach = 2.5 * F / (bwd_mean * 1e-3) / 1e12
-        traffic = profiled_traffic("fa_bwd_long.md", ["fa_bwd.cu", "ptx.cuh"])
+        traffic = profiled_traffic("fa_bwd_long.md", ["fa_bwd.cu", "ptx.cuh", "fa_internal.h"])
         kname = "fa_bwd (main + pre/post kernels, timed together)"
     else:
         ach = fwd_tf
-        traffic = profiled_traffic("fa_fwd_long.md", ["fa_fwd.cu", "ptx.cuh"])
+        traffic = profiled_traffic("fa_fwd_long.md", ["fa_fwd.cu", "ptx.cuh", "fa_internal.h"])
         kname = "fa_fwd_kernel"
     res["roofline"] = {"kernel": kname, "bound": "tensor", "achieved": round(ach, 2), "peak": peaks["bf16_tflops"],
                        "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4), "traffic": traffic,
@@ -409,6 +409,27 @@ def run_extra(peaks):
         pass
     out["varlen"] = r
     del x, o, lse
+    # window: B1 H32 N16384 d128, causal sliding window of 4096 keys (fwd and bwd)
+    w = synth.WORKLOADS["window"]
+    x = synth.make_dense(w.B, w.H, w.N, w.d, seed=0, device="cuda")
+    F = acc.masked_fwd_flops(w.B, w.H, w.N, w.N, w.d, *w.window)
+    o, lse = ops.fwd_masked(x["q"], x["k"], x["v"], window=w.window)
+    t_f = time_calls(torch, lambda: ops.fwd_masked(x["q"], x["k"], x["v"], window=w.window))
+    t_b = time_calls(torch, lambda: ops.bwd_masked(x["q"], x["k"], x["v"], o, lse, x["do"], window=w.window))
+    out["window"] = {"window": list(w.window), "fwd_ms": round(t_f, 4), "fwd_tflops": round(F / t_f / 1e9, 1),
+                     "bwd_ms": round(t_b, 4), "fwdbwd_tflops": round(2.5 * F / (t_f + t_b) / 1e9, 1),
+                     "flops": "visible scores only, 4d per score"}
+    del x, o, lse
+    # prefill: 8 chunks of 2048 queries against 16384-key caches, GQA 32:8, bottom-right causal
+    w = synth.WORKLOADS["prefill"]
+    x = synth.make_masked(w.B, w.N, w.n_k, w.H, w.h_kv, w.d, seed=0, device="cuda", with_do=False)
+    F = acc.masked_fwd_flops(w.B, w.H, w.N, w.n_k, w.d, *w.window)
+    ops.fwd_masked(x["q"], x["k"], x["v"], window=w.window)
+    t_f = time_calls(torch, lambda: ops.fwd_masked(x["q"], x["k"], x["v"], window=w.window))
+    out["prefill"] = {"fwd_ms": round(t_f, 4), "fwd_tflops": round(F / t_f / 1e9, 1),
+                      "flops": "visible scores only, 4d per score"}
+    del x
+    torch.cuda.empty_cache()
     # decode: B64 L32768 H32 d128 (34.4 GB of K/V, far larger than L2)
     w = synth.WORKLOADS["decode"]
     try:

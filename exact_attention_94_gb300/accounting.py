@@ -56,3 +56,22 @@ def idle_fraction(n_blocks: int, n_sm: int) -> float:
 def decode_bytes(B: int, H: int, L: int, d: int, elem_bytes: int = 2) -> float:
     """K and V cache bytes a decode step must stream once."""
     return 2.0 * B * H * L * d * elem_bytes
+
+
+def masked_visible_scores(n_q: int, n_k: int, window_left: int, window_right: int) -> int:
+    """Scores a bottom-right aligned mask leaves visible in one head: query i
+    sees keys [i + n_k - n_q - window_left, i + n_k - n_q + window_right]
+    clipped to the keys, a bound of -1 leaving its side open."""
+    total = 0
+    off = n_k - n_q
+    for i in range(n_q):
+        lo = 0 if window_left < 0 else max(0, i + off - window_left)
+        hi = n_k if window_right < 0 else min(n_k, i + off + window_right + 1)
+        total += max(0, hi - lo)
+    return total
+
+
+def masked_fwd_flops(B: int, H: int, n_q: int, n_k: int, d: int, window_left: int, window_right: int) -> float:
+    """Forward FLOPs over the visible scores only (two products of 2d each);
+    unlike fwd_flops' causal convention this counts the diagonal exactly."""
+    return 4.0 * d * B * H * masked_visible_scores(n_q, n_k, window_left, window_right)

@@ -143,9 +143,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) fa_decode_split_kernel(const D
   } else {
     // ============================================================ compute warps
     float qv[kDecHPW][E], o[kDecHPW][E], m_run[kDecHPW], l_lane[kDecHPW];
+    int kv_off[kDecHPW];  // element offset of this lane's slice of its K/V head within a staged key row
 #pragma unroll
     for (int j = 0; j < kDecHPW; ++j) {
       const int hj = warp + kDecWarps * j;
+      kv_off[j] = (hj / p.kv_group) * D + lane * E;
       m_run[j] = -INFINITY;
       l_lane[j] = 0.f;
 #pragma unroll
@@ -175,13 +177,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) fa_decode_split_kernel(const D
       for (int j = 0; j < kDecHPW; ++j) {
         const int hj = warp + kDecWarps * j;  // query head of the CTA
         if (hj >= Gq) break;
-        const int kvj = hj / p.kv_group;      // its K/V head of the CTA
         // partial dot products of this lane's elements for the 4 keys
         float part[kDecT];
 #pragma unroll
         for (int m = 0; m < kDecT; ++m) {
           float kf[E];
-          load_row<E>(ks + ((size_t)m * G + kvj) * D + lane * E, kf);
+          load_row<E>(ks + m * G * D + kv_off[j], kf);
           float acc = 0.f;
 #pragma unroll
           for (int e = 0; e < E; ++e) acc = fmaf(qv[j][e], kf[e], acc);
@@ -211,7 +212,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) fa_decode_split_kernel(const D
           if (m < nv) {
             const float pk = __shfl_sync(0xffffffffu, pm, (m >> 1) * 16 + (m & 1) * 8);
             float vf[E];
-            load_row<E>(vs + ((size_t)m * G + kvj) * D + lane * E, vf);
+            load_row<E>(vs + m * G * D + kv_off[j], vf);
 #pragma unroll
             for (int e = 0; e < E; ++e) o[j][e] = fmaf(pk, vf[e], o[j][e]);
           }

@@ -21,6 +21,13 @@ benchmark configurations state them):
 * ``varlen``  32 sequences, lengths uniform integers in [128, 4096], packed
   end to end, H=32 d=128, causal per sequence
 * ``decode``  B=64 single queries against a 32768-token KV cache, H=32 d=128
+* ``window``  B=1 H=32 N=16384 d=128, causal sliding window of 4096 keys
+  (window_left 4095); the pages give no size for a windowed run, so this one
+  is a long-context configuration of the usual 4096-token window
+* ``prefill`` chunked prefill: B=8 chunks of 2048 new queries against
+  16384-key caches, 32 query heads sharing 8 K/V heads, d=128, bottom-right
+  causal; sizes chosen here, the pages' example (4 queries, 128 keys) being
+  a toy
 """
 from __future__ import annotations
 
@@ -36,7 +43,7 @@ IDX_Q, IDX_K, IDX_V, IDX_DO, IDX_LENGTHS = 0, 1, 2, 3, 4
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str                 # "dense" | "varlen" | "decode"
+    kind: str                 # "dense" | "varlen" | "decode" | "masked"
     B: int                    # batch (dense/decode) or number of sequences (varlen)
     H: int
     N: int                    # sequence length (dense), KV cache length (decode), max length (varlen)
@@ -46,6 +53,9 @@ class Workload:
     len_lo: int = 0           # varlen: inclusive length range
     len_hi: int = 0
     seed: int = 0
+    n_k: int = 0              # keys per sequence when they differ from N (0 = N)
+    h_kv: int = 0             # K/V heads when fewer than H (0 = H)
+    window: tuple = (-1, -1)  # (window_left, window_right); (-1, 0) with causal
 
     @property
     def scale(self) -> float:
@@ -59,6 +69,8 @@ WORKLOADS = {
     "long": Workload("long", "dense", 2, 16, 8192, 128, True, k_boost=3.0),
     "varlen": Workload("varlen", "varlen", 32, 32, 4096, 128, True, len_lo=128, len_hi=4096),
     "decode": Workload("decode", "decode", 64, 32, 32768, 128, False),
+    "window": Workload("window", "masked", 1, 32, 16384, 128, True, window=(4095, 0)),
+    "prefill": Workload("prefill", "masked", 8, 32, 2048, 128, True, n_k=16384, h_kv=8, window=(-1, 0)),
 }
 
 

@@ -1,6 +1,7 @@
 """Work accounting pinned to the worked numbers the pages print."""
 import json
 import os
+import pytest
 
 from exact_attention_94_gb300 import accounting as acc
 
@@ -43,3 +44,15 @@ def test_flop_conventions():
     assert abs(f - 549.755813888e9) < 1
     assert acc.bwd_flops(2, 16, 8192, 128, True) == 2.5 * f
     assert acc.decode_bytes(64, 32, 32768, 128) == 2 * 64 * 32 * 32768 * 128 * 2
+
+
+@pytest.mark.parametrize("nq,nk,wl,wr", [(10, 10, -1, 0), (7, 30, 4, 1), (30, 7, -1, 0), (16, 16, -1, -1),
+                                         (50, 50, 9, 0), (12, 40, 3, -1), (5, 5, 0, 0)])
+def test_masked_visible_scores_count_the_oracle_mask(nq, nk, wl, wr):
+    import oracle
+    assert acc.masked_visible_scores(nq, nk, wl, wr) == int(oracle.window_visible(nq, nk, wl, wr).sum())
+
+
+def test_masked_flops_square_causal():
+    # the exact count includes the diagonal: N (N + 1) / 2 scores
+    assert acc.masked_fwd_flops(1, 1, 8, 8, 4, -1, 0) == 4 * 4 * 36
