@@ -13,3 +13,4 @@ from .masked import (  # noqa: F401
     window_visible, top_left_causal_visible, block_mask, head_forward_visible, head_backward_visible,
     masked_forward, masked_backward, masked_varlen_forward, masked_varlen_backward,
 )
+from . import fp8  # noqa: F401  (e4m3 block quantisation with incoherent processing)

@@ -220,3 +220,26 @@ def make_masked_varlen(lengths_q, lengths_k, Hq, Hkv, d, seed=0, device="cpu", w
     if with_do:
         out["do"] = randn_bf16((tq, Hq, d), seed, IDX_DO, device)
     return out
+
+
+IDX_SIGNS, IDX_OUTLIER_MASK, IDX_OUTLIER_VALUE = 5, 6, 7
+
+
+def hadamard_signs(d: int, seed: int = 0) -> torch.Tensor:
+    """The random +-1 diagonal of incoherent processing, drawn on the host:
+    int8 [d] of -1 / +1 with equal probability."""
+    bits = torch.randint(0, 2, (d,), generator=_gen(seed, IDX_SIGNS, "cpu"))
+    return (bits * 2 - 1).to(torch.int8)
+
+
+def outlier_bf16(shape, seed: int, idx: int, device: str = "cpu", frac: float = 0.001,
+                 outlier_std: float = 10.0) -> torch.Tensor:
+    """Entries N(0, 1) plus, on a fraction ``frac`` of them chosen independently,
+    an extra N(0, outlier_std^2) term; fp32 draws rounded to bf16.  The default
+    is the outlier test of the FP8 discussion (0.1% of entries, N(0, 100))."""
+    base = torch.randn(shape, generator=_gen(seed, idx, device), dtype=torch.float32, device=device)
+    g = _gen(seed * 7 + idx, IDX_OUTLIER_MASK, device)
+    mask = torch.rand(shape, generator=g, device=device) < frac
+    extra = torch.randn(shape, generator=_gen(seed * 7 + idx, IDX_OUTLIER_VALUE, device), dtype=torch.float32,
+                        device=device) * outlier_std
+    return (base + mask * extra).to(torch.bfloat16)
