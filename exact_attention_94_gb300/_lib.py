@@ -34,6 +34,8 @@ SIGNATURES = {
     "fa_fwd_masked_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P] + [_I] * 10 + [_F, _P]),
     "fa_bwd_masked": (_I, [_P] * 10 + [_I] * 8 + [_F, _P]),
     "fa_bwd_masked_varlen": (_I, [_P] * 12 + [_I] * 10 + [_F, _P]),
+    "fa_fp8_quantize": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "fa_fwd_fp8": (_I, [_P] * 8 + [_I] * 9 + [_F, _P]),
     "fa_decode_workspace_bytes": (_S, [_I, _I, _I, _I]),
     "fa_decode_num_splits": (_I, [_I, _I, _I, _I]),
     "fa_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _F, _P]),

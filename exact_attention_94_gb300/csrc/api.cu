@@ -84,6 +84,18 @@ bool make_tmap_bhnd(CUtensorMap* m, const void* ptr, int D, int n_rows, int H, i
   return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_u8(CUtensorMap* m, const void* ptr, const uint64_t dims_in[4], const uint64_t strides_in[3],
+                  int box_y) {
+  cuuint64_t dims[4] = {dims_in[0], dims_in[1], dims_in[2], dims_in[3]};
+  cuuint64_t strides[3] = {strides_in[0], strides_in[1], strides_in[2]};
+  cuuint32_t box[4] = {128, (cuuint32_t)box_y, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace fa
 
 using namespace fa;
@@ -417,6 +429,82 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
   // and overwrites the per-row arrays, so the previous call's contents never leak.
   return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, scratch, nullptr, nullptr, B, N, N, N, N, N, N, H, H, d, -1,
                     causal_right(causal), scale, stream);
+}
+
+// ---------------------------------------------------------------- FP8 forward
+
+fa_status fa_fp8_quantize(const void* x, const signed char* signs, void* codes, float* scales, int B, int N, int H, int d,
+                          int rotate, int transpose, fa_stream_t stream) {
+  if (B < 1 || H < 1 || N < 0 || (rotate != 0 && rotate != 1) || (transpose != 0 && transpose != 1))
+    return FA_ERR_INVALID_ARG;
+  if (!x || !codes || !scales || (rotate && !signs)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(codes) || (reinterpret_cast<uintptr_t>(scales) & 3u) != 0)
+    return FA_ERR_MISALIGNED;
+  if (B > 65535 || H > 65535) return FA_ERR_INVALID_ARG;
+  if (N == 0) return FA_OK;
+  if (!ensure_init()) return FA_ERR_LAUNCH;
+  cudaError_t e = launch_fp8_quantize(x, signs, static_cast<uint8_t*>(codes), scales, B, N, H, d, rotate != 0,
+                                      transpose != 0, (cudaStream_t)stream);
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+fa_status fa_fwd_fp8(const void* q_codes, const void* k_codes, const void* vt_codes, const float* q_scale,
+                     const float* k_scale, const float* v_scale, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+                     int Nk, int d, int window_left, int window_right, int rotated, float scale, fa_stream_t stream) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Nq < 0 || Nk < 1 || (rotated != 0 && rotated != 1))
+    return FA_ERR_INVALID_ARG;
+  if (!q_codes || !k_codes || !vt_codes || !q_scale || !k_scale || !v_scale || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  int wl = window_left, wr = window_right;
+  if (!scale_ok(scale) || !window_ok(wl, wr, Nq, Nk)) return FA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q_codes, k_codes, vt_codes, o, lse};
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) return FA_ERR_MISALIGNED;
+  if (((reinterpret_cast<uintptr_t>(q_scale) | reinterpret_cast<uintptr_t>(k_scale) |
+        reinterpret_cast<uintptr_t>(v_scale)) & 3u) != 0)
+    return FA_ERR_MISALIGNED;
+  if ((long long)B * Hq > 65535LL * 8) return FA_ERR_INVALID_ARG;
+  const int num_pairs = (Nq + 255) / 256;
+  if (num_pairs > 65535) return FA_ERR_INVALID_ARG;
+  if (Nq == 0) return FA_OK;
+  if (!ensure_init()) return FA_ERR_LAUNCH;
+  const int n_kblk = (Nk + 127) / 128;
+  const uint64_t n_pad = (uint64_t)n_kblk * 128;
+  CUtensorMap tq, tk, tvt;
+  const uint64_t dq[4] = {(uint64_t)d, (uint64_t)Nq, (uint64_t)Hq, (uint64_t)B};
+  const uint64_t sq[3] = {(uint64_t)Hq * d, (uint64_t)d, (uint64_t)Nq * Hq * d};
+  const uint64_t dk[4] = {(uint64_t)d, (uint64_t)Nk, (uint64_t)Hkv, (uint64_t)B};
+  const uint64_t sk[3] = {(uint64_t)Hkv * d, (uint64_t)d, (uint64_t)Nk * Hkv * d};
+  const uint64_t dv[4] = {n_pad, (uint64_t)d, (uint64_t)Hkv, (uint64_t)B};
+  const uint64_t sv[3] = {n_pad, n_pad * d, n_pad * d * Hkv};
+  if (!make_tmap_u8(&tq, q_codes, dq, sq, 128) || !make_tmap_u8(&tk, k_codes, dk, sk, 128) ||
+      !make_tmap_u8(&tvt, vt_codes, dv, sv, d))
+    return FA_ERR_INVALID_ARG;
+  FwdParams p{};
+  p.kv_group = Hq / Hkv;
+  p.o = o;
+  p.lse = lse;
+  p.H = Hq;
+  p.bh_total = B * Hq;
+  p.n_rows = Nq;
+  p.n_rows_k = Nk;
+  p.seq_len = Nq;
+  p.seq_len_k = Nk;
+  p.win_left = wl;
+  p.win_right = wr;
+  p.num_pairs = num_pairs;
+  p.q_scale = q_scale;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.n_qblk = (Nq + 127) / 128;
+  p.n_kblk = n_kblk;
+  p.scale_log2 = scale * kLog2e / (rotated ? (float)d : 1.f);
+  p.tau = g_opt.tau;
+  p.err = g_err_ptr;
+  p.timeout_ns = g_opt.timeout_ns;
+  cudaError_t e = launch_fwd_fp8(tq, tk, tvt, p, mask_kind(wl, wr), B * Hq, (cudaStream_t)stream);
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 size_t fa_decode_workspace_bytes(int B, int H, int d, int num_splits) {

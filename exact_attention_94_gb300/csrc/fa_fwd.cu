@@ -56,11 +56,12 @@ __device__ __forceinline__ float ex2_poly(float x) {
   return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
 }
 
-template <int D>
+template <int D, bool F8>
 struct FwdLayout {
-  static constexpr uint32_t kTile = 128u * D * 2u;   // one 128-row bf16 tile
-  static constexpr uint32_t kChunk = 128u * 128u;    // 128 rows x 64 bf16 (one 128-byte swizzle column)
-  static constexpr int kStages = D == 128 ? 4 : 8;    // K/V ring slots
+  static constexpr uint32_t kElt = F8 ? 1u : 2u;     // bytes per element
+  static constexpr uint32_t kTile = 128u * D * kElt; // one 128-row tile (a 128-key V^T tile for e4m3)
+  static constexpr uint32_t kChunk = 128u * 128u;    // 128 rows x 128 bytes (one 128-byte swizzle column)
+  static constexpr int kStages = (F8 || D == 64) ? 8 : 4;  // K/V ring slots
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kKVOff = 2 * kTile;
   static constexpr uint32_t kBarOff = kKVOff + kStages * kTile;
@@ -72,15 +73,16 @@ constexpr int kHeadGroup = 8;  // heads whose CTAs are scheduled together
 
 }  // namespace
 
-template <int D, int MASK, bool POLY>
+template <int D, int MASK, bool POLY, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using L = FwdLayout<D>;
+  using L = FwdLayout<D, F8>;
   constexpr bool MASKED = MASK != kMaskNone;
   constexpr bool LEFT = MASK == kMaskWindow;  // rows' keys may start after key 0
   constexpr int NS = L::kStages;
-  constexpr int CH = D / 64;
+  constexpr int CH = (int)(D * L::kElt / 128);  // 128-byte swizzle columns per row
+  constexpr int CHUNK_ELEMS = (int)(128 / L::kElt);
   constexpr uint32_t TILE = L::kTile;
   constexpr uint32_t CHUNK = L::kChunk;
 
@@ -187,7 +189,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(BAR(Q_FULL), 2 * TILE);
       for (int t = 0; t < 2; ++t)
         for (int c = 0; c < CH; ++c)
-          tma_load_4d(q_s + t * TILE + c * CHUNK, &tm_q, BAR(Q_FULL), c * 64, seq_start + q0 + 128 * t, h, b_coord);
+          tma_load_4d(q_s + t * TILE + c * CHUNK, &tm_q, BAR(Q_FULL), c * CHUNK_ELEMS, seq_start + q0 + 128 * t, h,
+                      b_coord);
       bool ok = true;
       for (int j = jmin; j < jmax && ok; ++j) {
         for (int which = 0; which < 2; ++which) {
@@ -198,10 +201,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(BAR(KV_FULL + slot), TILE);
+          if (F8 && which) {  // V^T codes: d rows of 128 keys
+            tma_load_4d(kv_s + slot * TILE, &tm_v, BAR(KV_FULL + slot), 128 * j, 0, h_kv, b_coord);
+            continue;
+          }
           const CUtensorMap* m = which ? &tm_v : &tm_k;
           for (int c = 0; c < CH; ++c)
-            tma_load_4d(kv_s + slot * TILE + c * CHUNK, m, BAR(KV_FULL + slot), c * 64, kv_start + 128 * j, h_kv,
-                        b_coord);
+            tma_load_4d(kv_s + slot * TILE + c * CHUNK, m, BAR(KV_FULL + slot), c * CHUNK_ELEMS, kv_start + 128 * j,
+                        h_kv, b_coord);
         }
       }
       if (!ok) {  // let copies already in flight land before the CTA's shared memory goes away
@@ -213,30 +220,42 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ============================================================ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t IDESC_O = idesc_bf16(128, D, false, true);
+      constexpr uint32_t IDESC_S = F8 ? idesc_e4m3(128, 128) : idesc_bf16(128, 128, false, false);
+      constexpr uint32_t IDESC_O = F8 ? idesc_e4m3(128, D) : idesc_bf16(128, D, false, true);
       const uint32_t tS0 = tmem, tS1 = tmem + 128;
       const uint32_t tO0 = tmem + 256, tO1 = tmem + 256 + D;
       bool ok = true;
 
-      // S_t = Q_t K^T: both operands K-major, 128-byte swizzle; K=16 per instruction
+      // S_t = Q_t K^T: both operands K-major, 128-byte swizzle; each instruction
+      // covers 32 bytes of K (16 bf16 or 32 e4m3 elements)
       auto issue_S = [&](int t, int slot) {
         const uint32_t qa = q_s + t * TILE, ka = kv_s + slot * TILE;
         const uint32_t dst = t ? tS1 : tS0;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < (int)(D * L::kElt / 32); ++kk) {
           const uint32_t off = (kk / 4) * CHUNK + (kk % 4) * 32;
-          mma_ss(dst, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024), IDESC_S, kk > 0);
+          if constexpr (F8)
+            mma_ss_f8(dst, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024), IDESC_S, kk > 0);
+          else
+            mma_ss(dst, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024), IDESC_S, kk > 0);
         }
       };
-      // O_t += P_t V: P from TMEM (bf16 pairs over S_t's columns), V MN-major from shared memory
+      // O_t += P_t V with P from TMEM over S_t's columns.  bf16: pairs per column,
+      // V MN-major; e4m3: four per column, V^T K-major (d rows of 128 keys).
       auto issue_PV = [&](int t, int slot, bool acc) {
         const uint32_t va = kv_s + slot * TILE;
         const uint32_t dst = t ? tO1 : tO0;
         const uint32_t pa = t ? tS1 : tS0;
+        if constexpr (F8) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(dst, pa + kk * 8, smem_desc_sw128(va + kk * 2048, CHUNK, 1024), IDESC_O, (acc || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts_f8(dst, pa + kk * 8, smem_desc_sw128(va + kk * 32, 16, 1024), IDESC_O, (acc || kk > 0) ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(dst, pa + kk * 8, smem_desc_sw128(va + kk * 2048, CHUNK, 1024), IDESC_O,
+                   (acc || kk > 0) ? 1u : 0u);
+        }
       };
 
       ok = mbar_wait(BAR(Q_FULL), 0, w, 2);
@@ -313,8 +332,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int key_lo = LEFT ? mask_key_lo(row, seq_len, kv_len, p.win_left) : 0;
     const int key_hi = MASKED ? mask_key_hi(row, seq_len, kv_len, p.win_right) : kv_len;
     const int jlo = t ? jlo1 : jlo0, jhi = t ? jhi1 : jhi0;
+    // e4m3 operands: scores of key tile j are dequantised by sq (this query
+    // tile's scale) * sk_j; P of tile j is multiplied by sv_j / sv_ref before
+    // its rounding to e4m3 (sv_ref = the head's largest V scale, so P stays in
+    // [0, 2^tau]) and O by sv_ref at the end.  The factor goes into the
+    // exponent, and l adds P back at its own scale.
+    float sl2_q = sl2, sv_ref = 1.f;
+    const float* k_sc = nullptr;
+    const float* v_sc = nullptr;
+    if constexpr (F8) {
+      const size_t hk = (size_t)b * (p.H / p.kv_group) + h_kv;
+      const int qb = (q0 >> 7) + t;  // past the last block only when this tile has no rows
+      sl2_q = qb < p.n_qblk ? sl2 * p.q_scale[((size_t)b * p.H + h) * p.n_qblk + qb] : 0.f;
+      k_sc = p.k_scale + hk * p.n_kblk;
+      v_sc = p.v_scale + hk * p.n_kblk;
+      float mv = 0.f;
+      for (int i = lane; i < p.n_kblk; i += 32) mv = fmaxf(mv, v_sc[i]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, o));
+      sv_ref = mv > 0.f ? mv : 1.f;
+    }
 
     for (int j = jlo; j < jhi; ++j) {
+      float sl2j = sl2, lrv = 0.f, inv_rv = 1.f;
+      if constexpr (F8) {
+        // an all-zero Q or K block (scale 0) has all-zero codes, so its scores are
+        // exactly 0 under any positive multiplier; a positive one keeps masked
+        // -inf scores at -inf instead of turning them into NaN
+        sl2j = fmaxf(sl2_q * k_sc[j], 1e-30f);
+        const float rv = fmaxf(v_sc[j] / sv_ref, 0x1p-30f);  // a zero block's P rounds to 0 either way
+        lrv = log2f(rv);
+        inv_rv = 1.f / rv;
+      }
       ok = mbar_wait(BAR(S_FULL + t), (j - jlo) & 1, w, 7);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
@@ -345,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mg[g] = m;
       }
       const float mx = max3f(max3f(mg[0], mg[1], mg[2]), max3f(mg[3], mg[4], mg[5]), fmaxf(mg[6], mg[7]));
-      const float m_new = mx * sl2;
+      const float m_new = mx * sl2j;
       float alpha = 1.f;
       const bool resc = m_new > m_ref + tau;
       if (resc) {
@@ -355,10 +404,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
 
       // p = 2^(x * scale * log2 e - m_ref): packed FMA, exponentials, packed partial sums
-      const uint64_t sl2x2 = f2_pack(sl2, sl2);
-      const uint64_t nmb2 = f2_pack(-mb, -mb);
+      const uint64_t sl2x2 = f2_pack(sl2j, sl2j);
+      const uint64_t nmb2 = f2_pack(lrv - mb, lrv - mb);
       uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
       uint32_t pk[2][32];
+      float ph0 = 0.f, ph1 = 0.f;  // e4m3: the previous pair, packed with the next into one word
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
         float y0, y1;
@@ -372,15 +422,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           p1 = ex2_sfu(y1);
         }
         acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
-        pk[i / 32][i % 32] = pack_bf16x2(p0, p1);
-        if (i == 31) tmem_st32(tS, pk[0]);  // first half of P out early: frees registers
+        if constexpr (F8) {
+          if (i & 1)
+            pk[0][i / 2] = pack_e4m3x4(ph0, ph1, p0, p1);  // keys 4c..4c+3 in column c
+          else
+            ph0 = p0, ph1 = p1;
+        } else {
+          pk[i / 32][i % 32] = pack_bf16x2(p0, p1);
+          if (i == 31) tmem_st32(tS, pk[0]);  // first half of P out early: frees registers
+        }
       }
       float s0, s1, s2, s3, s4, s5, s6, s7;
       f2_unpack(acc[0], s0, s1);
       f2_unpack(acc[1], s2, s3);
       f2_unpack(acc[2], s4, s5);
       f2_unpack(acc[3], s6, s7);
-      l = l * alpha + (((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7)));
+      l = l * alpha + (((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7))) * inv_rv;
 
       if (j > jlo && __any_sync(0xffffffffu, resc)) {
         // rows whose reference moved: O~ *= alpha (alpha = 1 for the others)
@@ -394,7 +451,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(tO + 32 * c, ov);
         }
       }
-      tmem_st32(tS + 32, pk[1]);
+      if constexpr (F8)
+        tmem_st32(tS, pk[0]);  // the whole tile's P: 32 columns of four e4m3 each
+      else
+        tmem_st32(tS + 32, pk[1]);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(BAR(P_FULL + t));
@@ -417,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = mbar_wait(BAR(O_FINAL + t), 0, w, 8);
       if (__all_sync(0xffffffffu, ok)) {
         tc_fence_after();
-        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        const float inv_l = l > 0.f ? sv_ref / l : 0.f;  // sv_ref = 1 unless e4m3
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t ov[32];
@@ -447,11 +507,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, int MASK, bool POLY>
+template <int D, int MASK, bool POLY, bool F8>
 static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const FwdParams& p, int grid_x, cudaStream_t stream) {
-  auto kern = fa_fwd_kernel<D, MASK, POLY>;
-  constexpr uint32_t smem = FwdLayout<D>::kBytes;
+  auto kern = fa_fwd_kernel<D, MASK, POLY, F8>;
+  constexpr uint32_t smem = FwdLayout<D, F8>::kBytes;
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -467,7 +527,7 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                        int D, int mask, bool poly, int grid_x, cudaStream_t stream) {
 #define FA_FWD_CASE(DD, MM, PP) \
-  if (D == DD && mask == MM && poly == PP) return launch_fwd_t<DD, MM, PP>(tq, tk, tv, p, grid_x, stream);
+  if (D == DD && mask == MM && poly == PP) return launch_fwd_t<DD, MM, PP, false>(tq, tk, tv, p, grid_x, stream);
 #define FA_FWD_CASES(DD)         \
   FA_FWD_CASE(DD, kMaskNone, false)   \
   FA_FWD_CASE(DD, kMaskNone, true)    \
@@ -479,6 +539,14 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   FA_FWD_CASES(128)
 #undef FA_FWD_CASES
 #undef FA_FWD_CASE
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt, const FwdParams& p,
+                           int mask, int grid_x, cudaStream_t stream) {
+  if (mask == kMaskNone) return launch_fwd_t<128, kMaskNone, false, true>(tq, tk, tvt, p, grid_x, stream);
+  if (mask == kMaskRight) return launch_fwd_t<128, kMaskRight, false, true>(tq, tk, tvt, p, grid_x, stream);
+  if (mask == kMaskWindow) return launch_fwd_t<128, kMaskWindow, false, true>(tq, tk, tvt, p, grid_x, stream);
   return cudaErrorInvalidValue;
 }
 

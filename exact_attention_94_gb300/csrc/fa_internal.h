@@ -24,7 +24,14 @@ struct FwdParams {
   int win_left;              // mask (used by the masked kernels): query i sees keys
   int win_right;             //   [i + Nk - Nq - win_left, i + Nk - Nq + win_right]; -1 = unbounded side
   int num_pairs;             // grid.y: pairs of 128-row query tiles per (sequence, head)
-  float scale_log2;          // scale * log2(e)
+  // e4m3 operands only: one scale per 128-row block, [B][H][n_qblk] for Q and
+  // [B][Hkv][n_kblk] for K and V (V's codes are stored transposed per head)
+  const float* q_scale;
+  const float* k_scale;
+  const float* v_scale;
+  int n_qblk;
+  int n_kblk;
+  float scale_log2;          // scale * log2(e) (e4m3 with rotated Q, K: also divided by d)
   float tau;                 // lazy-rescale threshold, log2 units
   unsigned* err;             // device error word
   unsigned long long timeout_ns;
@@ -72,6 +79,22 @@ inline int mask_kind(int win_left, int win_right) {
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                        int D, int mask, bool poly, int grid_x, cudaStream_t stream);
+
+// Forward on e4m3 operands (d = 128): tq, tk over codes [B][N][H][d] (uint8),
+// tv over V's codes transposed [B][Hkv][d][n_pad].
+cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt, const FwdParams& p,
+                           int mask, int grid_x, cudaStream_t stream);
+
+// Block quantisation to e4m3 (d = 64 or 128): x [B][N][H][d] bf16 -> codes and
+// one fp32 scale per 128-row block [B][H][ceil(N/128)].  rotate: multiply each
+// row by the Hadamard matrix (fast transform) and then by signs[d] (+-1).
+// transpose: codes laid out [B][H][d][n_pad] (n_pad = blocks * 128, zero-filled).
+cudaError_t launch_fp8_quantize(const void* x, const int8_t* signs, uint8_t* codes, float* scales, int B, int N,
+                                int H, int d, bool rotate, bool transpose, cudaStream_t stream);
+
+// 4-D uint8 tensor map: extents dims[0..3] (dims[0] innermost, contiguous),
+// byte strides of dims 1..3, a 128 x box_y box, 128-byte swizzle.
+bool make_tmap_u8(CUtensorMap* m, const void* ptr, const uint64_t dims[4], const uint64_t strides[3], int box_y);
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const BwdParams& p, int D, int mask, cudaStream_t stream);

@@ -371,3 +371,61 @@ def bwd_masked_varlen(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seq
                                     Hq, Hkv, d, wl, wr, scale, _stream(stream))
     _lib.check(st, "fa_bwd_masked_varlen")
     return dq, dk, dv
+
+
+# ---------------------------------------------------------------- FP8 forward
+
+def fp8_quantize(x, signs=None, transpose: bool = False, stream=None):
+    """e4m3 block quantisation of x [B, N, H, d] (bf16).  With ``signs`` (int8
+    [d] of +-1 on the device) the rows are first rotated by the Hadamard matrix
+    and the signs.  Returns (codes uint8 [B, N, H, d], or [B, H, d, n_pad] when
+    transposed; scales fp32 [B, H, ceil(N / 128)])."""
+    _check_bf16("x", x)
+    B, N, H, d = x.shape
+    nblk = (N + 127) // 128
+    if signs is not None:
+        if signs.dtype != torch.int8 or tuple(signs.shape) != (d,) or signs.device != x.device:
+            raise ValueError("signs must be int8 [d] on the device of x")
+    if transpose:
+        codes = torch.empty((B, H, d, nblk * 128), dtype=torch.uint8, device=x.device)
+    else:
+        codes = torch.empty((B, N, H, d), dtype=torch.uint8, device=x.device)
+    scales = torch.empty((B, H, nblk), dtype=torch.float32, device=x.device)
+    st = lib().fa_fp8_quantize(_ptr(x), _ptr(signs), _ptr(codes), _ptr(scales), B, N, H, d,
+                               int(signs is not None), int(bool(transpose)), _stream(stream))
+    _lib.check(st, "fa_fp8_quantize")
+    return codes, scales
+
+
+def fwd_fp8_codes(q_codes, k_codes, vt_codes, q_scale, k_scale, v_scale, causal: bool = False,
+                  window: Optional[Tuple[int, int]] = None, rotated: bool = True, scale: Optional[float] = None,
+                  stream=None):
+    """Attention on e4m3 operands from fp8_quantize (V transposed).
+    Returns (o [B, Nq, Hq, d] bf16, lse [B, Hq, Nq])."""
+    B, Nq, Hq, d = q_codes.shape
+    Nk, Hkv = k_codes.shape[1], k_codes.shape[2]
+    for name, t in (("q_codes", q_codes), ("k_codes", k_codes), ("vt_codes", vt_codes)):
+        if t.dtype != torch.uint8 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous uint8 CUDA tensor")
+    if tuple(vt_codes.shape) != (B, Hkv, d, (Nk + 127) // 128 * 128):
+        raise ValueError("vt_codes must be [B, Hkv, d, ceil(Nk / 128) * 128]")
+    wl, wr = _window(causal, window)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty((B, Nq, Hq, d), dtype=torch.bfloat16, device=q_codes.device)
+    l = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q_codes.device)
+    st = lib().fa_fwd_fp8(_ptr(q_codes), _ptr(k_codes), _ptr(vt_codes), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
+                          _ptr(o), _ptr(l), B, Hq, Hkv, Nq, Nk, d, wl, wr, int(bool(rotated)), scale,
+                          _stream(stream))
+    _lib.check(st, "fa_fwd_fp8")
+    return o, l
+
+
+def fwd_fp8(q, k, v, signs=None, causal: bool = False, window: Optional[Tuple[int, int]] = None,
+            scale: Optional[float] = None, stream=None):
+    """The FP8 forward from bf16 inputs: quantise Q and K (rotated when signs
+    are given) and V (transposed), then attend.  Returns (o, lse)."""
+    qc, qs = fp8_quantize(q, signs, stream=stream)
+    kc, ks = fp8_quantize(k, signs, stream=stream)
+    vc, vs = fp8_quantize(v, None, transpose=True, stream=stream)
+    return fwd_fp8_codes(qc, kc, vc, qs, ks, vs, causal=causal, window=window, rotated=signs is not None,
+                         scale=scale, stream=stream)

@@ -208,6 +208,45 @@ fa_status fa_bwd_masked_varlen(const void* q, const void* k, const void* v, cons
                                int window_right, float scale, fa_stream_t stream);
 
 /*
+ * FP8 forward, step 1: block quantisation to e4m3 ("efficient-attention/
+ * flash-2-3", section "FP8, and the outlier problem": one scale per block of
+ * Q, K and V; Q and K first multiplied by a Hadamard matrix times a random
+ * +-1 diagonal, "incoherent processing", which spreads outliers over all
+ * coordinates).  A block is 128 consecutive rows of one (batch, head).
+ *   x         : [B, N, H, d] bf16, device
+ *   signs     : int8 [d] of -1 / +1, device (required when rotate = 1)
+ *   rotate    : 1 = rows become (x H) * signs, H the Sylvester-Hadamard matrix
+ *               with entries +-1 (fast transform in fp32); 0 = as they are
+ *   codes     : uint8, written: [B, N, H, d] (transpose = 0), or per head
+ *               [B, H, d, n_pad] with n_pad = ceil(N / 128) * 128 and the rows
+ *               past N zero (transpose = 1, the layout fa_fwd_fp8 takes for V)
+ *   scales    : fp32 [B, H, ceil(N / 128)], written: amax / 448 of each block
+ *               (0 for an all-zero block); code = e4m3(x / scale), rounded to
+ *               nearest even and saturated at +-448
+ * d = 64 or 128; x and codes 16-byte aligned, scales 4-byte aligned.
+ */
+fa_status fa_fp8_quantize(const void* x, const signed char* signs, void* codes, float* scales, int B, int N, int H,
+                          int d, int rotate, int transpose, fa_stream_t stream);
+
+/*
+ * FP8 forward, step 2: attention on e4m3 operands (d = 128).  Both products
+ * run on the tensor cores in e4m3 with fp32 accumulation; P is rounded to
+ * e4m3 (after scaling by its key block's V scale over the head's largest V
+ * scale) before the P V product.  Scores are dequantised per pair of tiles,
+ * s = (q8 . k8) * q_scale * k_scale * scale (/ d when rotated, since
+ * H H^T = d I), and the mask is that of fa_fwd_masked.
+ *   q_codes  : [B, Nq, Hq, d] uint8 from fa_fp8_quantize (rotate as "rotated")
+ *   k_codes  : [B, Nk, Hkv, d] uint8, same rotation and signs as Q
+ *   vt_codes : [B, Hkv, d, ceil(Nk / 128) * 128] uint8 (V, transpose = 1, not rotated)
+ *   q_scale, k_scale, v_scale : their block scales
+ *   o        : [B, Nq, Hq, d] bf16, written;  lse : [B, Hq, Nq] fp32, written
+ * Returns FA_ERR_UNSUPPORTED for d != 128; otherwise as fa_fwd_masked.
+ */
+fa_status fa_fwd_fp8(const void* q_codes, const void* k_codes, const void* vt_codes, const float* q_scale,
+                     const float* k_scale, const float* v_scale, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+                     int Nk, int d, int window_left, int window_right, int rotated, float scale, fa_stream_t stream);
+
+/*
  * Size of the built-in scratch of fa_bwd_noalloc: 32 MiB of device memory,
  * compiled into the library and held by every GPU that loads it until the
  * process exits.
