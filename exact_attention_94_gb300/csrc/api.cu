@@ -503,7 +503,7 @@ fa_status fa_fwd_fp8(const void* q_codes, const void* k_codes, const void* vt_co
   p.tau = g_opt.tau;
   p.err = g_err_ptr;
   p.timeout_ns = g_opt.timeout_ns;
-  cudaError_t e = launch_fwd_fp8(tq, tk, tvt, p, mask_kind(wl, wr), B * Hq, (cudaStream_t)stream);
+  cudaError_t e = launch_fwd_fp8(tq, tk, tvt, p, mask_kind(wl, wr), g_opt.poly, B * Hq, (cudaStream_t)stream);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

@@ -5,15 +5,16 @@
 // matrix times a random +-1 diagonal before quantising).
 //
 // One CTA per 128-row block of one (batch, head); warp w owns rows
-// 16w .. 16w+15, lane l the d/32 consecutive columns l*d/32 ... of each row.
+// 16w .. 16w+15, a row is spread over d/16 lanes of 16 consecutive columns.
 //   rotate:   x <- (x H) * signs, H the Sylvester-Hadamard matrix (entries
 //             +-1), by the fast transform: stage widths 1, 2, 4, ..., d/2, each
-//             butterfly (a, b) -> (a + b, a - b) in fp32.  Widths below d/32
+//             butterfly (a, b) -> (a + b, a - b) in fp32.  Widths below 16
 //             stay inside a lane, the others pair lanes with shuffles.
 //   scale:    amax / 448 over the block (fp32, correctly rounded); 0 for an
 //             all-zero block, whose codes are 0.
-//   codes:    e4m3(x / scale), the division correctly rounded, the conversion
-//             rounding to nearest even and saturating.
+//   codes:    e4m3(x * (1 / scale)), the reciprocal and the product each
+//             correctly rounded, the conversion rounding to nearest even and
+//             saturating.
 //   layout:   codes [B][N][H][d] like the input, or (V) transposed per head,
 //             [B][H][d][n_pad], n_pad = blocks * 128, rows past N zero, so
 //             that the P V product reads V^T K-major.
@@ -24,15 +25,17 @@ namespace fa {
 
 namespace {
 
-constexpr int kQuantThreads = 256;
-constexpr int kRowsPerWarp = 16;
+constexpr int kQuantThreads = 256;  // 8 warps; each takes 16 rows of the 128-row block
+constexpr int kElems = 16;          // consecutive elements per lane
 
-template <int E>
-__device__ __forceinline__ void fwht_row(float (&v)[E], int lane) {
+// Butterflies of widths 1 .. 8 inside the lane's 16 elements, then widths
+// 16 * hl with the lane that differs in bit hl (hl < lanes per row).
+template <int LPR>
+__device__ __forceinline__ void fwht_row16(float (&v)[kElems], int lane) {
 #pragma unroll
-  for (int h = 1; h < E; h <<= 1) {
+  for (int h = 1; h < kElems; h <<= 1) {
 #pragma unroll
-    for (int i = 0; i < E; ++i) {
+    for (int i = 0; i < kElems; ++i) {
       if (!(i & h)) {
         const float a = v[i], b = v[i + h];
         v[i] = a + b;
@@ -41,10 +44,10 @@ __device__ __forceinline__ void fwht_row(float (&v)[E], int lane) {
     }
   }
 #pragma unroll
-  for (int hl = 1; hl < 32; hl <<= 1) {  // width E * hl: the partner lane differs in bit hl
+  for (int hl = 1; hl < LPR; hl <<= 1) {
     const bool upper = (lane & hl) != 0;
 #pragma unroll
-    for (int i = 0; i < E; ++i) {
+    for (int i = 0; i < kElems; ++i) {
       const float o = __shfl_xor_sync(0xffffffffu, v[i], hl);
       v[i] = upper ? (o - v[i]) : (v[i] + o);
     }
@@ -59,40 +62,49 @@ __global__ void __launch_bounds__(kQuantThreads) fa_fp8_quant_kernel(const __nv_
                                                                      uint8_t* __restrict__ codes,
                                                                      float* __restrict__ scales, int N, int H,
                                                                      int nblk) {
-  constexpr int E = D / 32;
+  constexpr int LPR = D / kElems;   // lanes per row
+  constexpr int RPI = 32 / LPR;     // rows per warp and iteration
+  constexpr int IT = 16 / RPI;      // iterations: 16 rows per warp
   const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int seg = lane % LPR;       // which 16 columns of the row
+  const int sub = lane / LPR;       // which row of the iteration
   __shared__ float s_amax[kQuantThreads / 32];
-  __shared__ __align__(16) uint8_t s_t[TR ? D * 128 : 16];
+  __shared__ __align__(16) uint8_t s_rows[TR ? 128 * D : 16];  // codes, row-major, for the transposed store
 
-  float sg[E];
+  uint32_t neg = 0;  // bit e: column seg*16 + e takes the sign -1
+  if (ROT) {
 #pragma unroll
-  for (int e = 0; e < E; ++e) sg[e] = ROT ? (float)signs[lane * E + e] : 1.f;
+    for (int e = 0; e < kElems; ++e) neg |= (signs[seg * kElems + e] < 0 ? 1u : 0u) << e;
+  }
 
-  float v[kRowsPerWarp][E];
+  float v[IT][kElems];
   float amax = 0.f;
 #pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r) {
-    const int n = blk * 128 + warp * kRowsPerWarp + r;
+  for (int it = 0; it < IT; ++it) {
+    const int n = blk * 128 + warp * 16 + it * RPI + sub;
     if (n < N) {
-      const __nv_bfloat16* src = x + (((size_t)b * N + n) * H + h) * D + lane * E;
+      const uint4* src = reinterpret_cast<const uint4*>(x + (((size_t)b * N + n) * H + h) * D + seg * kElems);
+      const uint4 w0 = src[0], w1 = src[1];
+      const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-      for (int e = 0; e < E; e += 2) {
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(src + e));
-        v[r][e] = f.x;
-        v[r][e + 1] = f.y;
+      for (int i = 0; i < 8; ++i) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[i]));
+        v[it][2 * i] = f.x;
+        v[it][2 * i + 1] = f.y;
       }
     } else {
 #pragma unroll
-      for (int e = 0; e < E; ++e) v[r][e] = 0.f;
+      for (int e = 0; e < kElems; ++e) v[it][e] = 0.f;
     }
     if (ROT) {
-      fwht_row<E>(v[r], lane);
+      fwht_row16<LPR>(v[it], lane);
 #pragma unroll
-      for (int e = 0; e < E; ++e) v[r][e] *= sg[e];
+      for (int e = 0; e < kElems; ++e)  // times -1: flip the sign bit
+        v[it][e] = __uint_as_float(__float_as_uint(v[it][e]) ^ (((neg >> e) & 1u) << 31));
     }
 #pragma unroll
-    for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(v[r][e]));
+    for (int e = 0; e < kElems; ++e) amax = fmaxf(amax, fabsf(v[it][e]));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -102,39 +114,45 @@ __global__ void __launch_bounds__(kQuantThreads) fa_fp8_quant_kernel(const __nv_
 #pragma unroll
   for (int i = 1; i < kQuantThreads / 32; ++i) amax = fmaxf(amax, s_amax[i]);
   const float scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 0.f;
+  const float inv = amax > 0.f ? __frcp_rn(scale) : 0.f;  // codes = e4m3(x * (1 / scale))
   if (threadIdx.x == 0) scales[((size_t)b * H + h) * nblk + blk] = scale;
 
 #pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r) {
-    const int rr = warp * kRowsPerWarp + r;  // row within the block
+  for (int it = 0; it < IT; ++it) {
+    const int rr = warp * 16 + it * RPI + sub;  // row within the block
     const int n = blk * 128 + rr;
-    float y[E];
+    uint32_t wd[4];
 #pragma unroll
-    for (int e = 0; e < E; ++e) y[e] = scale > 0.f ? __fdiv_rn(v[r][e], scale) : 0.f;
-    uint32_t word;
-    if constexpr (E == 4)
-      word = pack_e4m3x4(y[0], y[1], y[2], y[3]);
-    else
-      word = pack_e4m3x4(y[0], y[1], 0.f, 0.f);
+    for (int q = 0; q < 4; ++q)
+      wd[q] = pack_e4m3x4(__fmul_rn(v[it][4 * q], inv), __fmul_rn(v[it][4 * q + 1], inv),
+                          __fmul_rn(v[it][4 * q + 2], inv), __fmul_rn(v[it][4 * q + 3], inv));
+    uint4 word = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+    if (!(amax > 0.f)) word = make_uint4(0u, 0u, 0u, 0u);  // all-zero block: +0 codes (not -0 from flipped zeros)
     if constexpr (TR) {
-      if (n >= N) word = 0u;  // padding rows: +0 (a rotated zero row would give -0 codes)
-#pragma unroll
-      for (int e = 0; e < E; ++e) s_t[(lane * E + e) * 128 + rr] = (uint8_t)(word >> (8 * e));
+      if (n >= N) word = make_uint4(0u, 0u, 0u, 0u);  // padding rows: +0 (a rotated zero row would give -0)
+      *reinterpret_cast<uint4*>(s_rows + rr * D + seg * kElems) = word;
     } else if (n < N) {
-      uint8_t* dst = codes + (((size_t)b * N + n) * H + h) * D + lane * E;
-      if constexpr (E == 4)
-        *reinterpret_cast<uint32_t*>(dst) = word;
-      else
-        *reinterpret_cast<uint16_t*>(dst) = (uint16_t)word;
+      *reinterpret_cast<uint4*>(codes + (((size_t)b * N + n) * H + h) * D + seg * kElems) = word;
     }
   }
   if constexpr (TR) {
+    // thread -> column c, half of the rows: gather 64 bytes of column c and
+    // write them as one contiguous run of row c of V^T
     __syncthreads();
     const size_t n_pad = (size_t)nblk * 128;
-    for (int i = threadIdx.x; i < D * 8; i += kQuantThreads) {  // D rows of 128 bytes, 16 bytes each
-      const int c = i >> 3, part = i & 7;
-      const uint4 val = *reinterpret_cast<const uint4*>(s_t + c * 128 + part * 16);
-      *reinterpret_cast<uint4*>(codes + (((size_t)b * H + h) * D + c) * n_pad + (size_t)blk * 128 + part * 16) = val;
+    for (int i = threadIdx.x; i < D * 2; i += kQuantThreads) {
+      const int c = i % D, half = i / D;
+      uint32_t w[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int r0 = half * 64 + 4 * k;
+        w[k] = (uint32_t)s_rows[r0 * D + c] | ((uint32_t)s_rows[(r0 + 1) * D + c] << 8) |
+               ((uint32_t)s_rows[(r0 + 2) * D + c] << 16) | ((uint32_t)s_rows[(r0 + 3) * D + c] << 24);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(codes + (((size_t)b * H + h) * D + c) * n_pad + (size_t)blk * 128 +
+                                            half * 64);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
     }
   }
 }

@@ -543,10 +543,16 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
 }
 
 cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt, const FwdParams& p,
-                           int mask, int grid_x, cudaStream_t stream) {
-  if (mask == kMaskNone) return launch_fwd_t<128, kMaskNone, false, true>(tq, tk, tvt, p, grid_x, stream);
-  if (mask == kMaskRight) return launch_fwd_t<128, kMaskRight, false, true>(tq, tk, tvt, p, grid_x, stream);
-  if (mask == kMaskWindow) return launch_fwd_t<128, kMaskWindow, false, true>(tq, tk, tvt, p, grid_x, stream);
+                           int mask, bool poly, int grid_x, cudaStream_t stream) {
+#define FA_FP8_CASE(MM, PP) \
+  if (mask == MM && poly == PP) return launch_fwd_t<128, MM, PP, true>(tq, tk, tvt, p, grid_x, stream);
+  FA_FP8_CASE(kMaskNone, false)
+  FA_FP8_CASE(kMaskNone, true)
+  FA_FP8_CASE(kMaskRight, false)
+  FA_FP8_CASE(kMaskRight, true)
+  FA_FP8_CASE(kMaskWindow, false)
+  FA_FP8_CASE(kMaskWindow, true)
+#undef FA_FP8_CASE
   return cudaErrorInvalidValue;
 }
 

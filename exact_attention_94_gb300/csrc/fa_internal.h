@@ -83,7 +83,7 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
 // Forward on e4m3 operands (d = 128): tq, tk over codes [B][N][H][d] (uint8),
 // tv over V's codes transposed [B][Hkv][d][n_pad].
 cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt, const FwdParams& p,
-                           int mask, int grid_x, cudaStream_t stream);
+                           int mask, bool poly, int grid_x, cudaStream_t stream);
 
 // Block quantisation to e4m3 (d = 64 or 128): x [B][N][H][d] bf16 -> codes and
 // one fp32 scale per 128-row block [B][H][ceil(N/128)].  rotate: multiply each

@@ -21,8 +21,11 @@ Readings (the page gives the ideas, not the arithmetic):
     bias 7, subnormal spacing 2^-9; conversion rounds to nearest, ties to even,
     and saturates at +-448.
   * A block is 128 consecutive rows of one (batch, head) with all d columns.
-    Its scale is amax / 448 in float32 (1 for an all-zero block) and a code is
-    e4m3(x / scale) with the division in float32.
+    Its scale is amax / 448 in float32 and a code is e4m3(x * (1 / scale)),
+    the reciprocal and the product each rounded to float32 (a quantiser
+    multiplies by the inverse scale, as dequantisation multiplies by the
+    scale); an all-zero block has scale 0 and codes 0 (so that it contributes
+    nothing and never sets a reference scale).
   * R = H D with H the d x d Sylvester-Hadamard matrix (entries +-1, not
     normalised) and D = diag(signs): a row x becomes (x H) * signs.  The fast
     transform runs in float32, stage widths 1, 2, 4, ..., d/2, each butterfly
@@ -130,9 +133,12 @@ def quantize_rows(x32, block_rows: int = BLOCK_ROWS):
     for t in range(nblk):
         blk = x32[t * block_rows:(t + 1) * block_rows]
         amax = np.float32(np.max(np.abs(blk))) if blk.size else np.float32(0)
-        sc = np.float32(amax / np.float32(E4M3_MAX)) if amax > 0 else np.float32(1.0)
+        if amax == 0:  # all-zero block: scale 0, codes 0
+            continue
+        sc = np.float32(amax / np.float32(E4M3_MAX))
+        inv = np.float32(np.float32(1.0) / sc)
         scales[t] = sc
-        codes[t * block_rows:(t + 1) * block_rows] = e4m3_encode((blk / sc).astype(np.float32))
+        codes[t * block_rows:(t + 1) * block_rows] = e4m3_encode((blk * inv).astype(np.float32))
     return codes, scales
 
 
@@ -185,7 +191,8 @@ def per_tensor_quantize(x, signs: Optional[np.ndarray] = None):
         x = rotate_f32(x, signs)
     amax = np.float32(np.max(np.abs(x)))
     sc = np.float32(amax / np.float32(E4M3_MAX)) if amax > 0 else np.float32(1.0)
-    return e4m3_decode(e4m3_encode((x / sc).astype(np.float32))) * np.float64(sc)
+    inv = np.float32(np.float32(1.0) / sc)
+    return e4m3_decode(e4m3_encode((x * inv).astype(np.float32))) * np.float64(sc)
 
 
 def fp8_forward_variant(q, k, v, scale: float, causal: bool, signs: Optional[np.ndarray], block: bool):
