@@ -14,3 +14,4 @@ from .masked import (  # noqa: F401
     masked_forward, masked_backward, masked_varlen_forward, masked_varlen_backward,
 )
 from . import fp8  # noqa: F401  (e4m3 block quantisation with incoherent processing)
+from . import paged  # noqa: F401  (write side of the paged cache: append, free list, copy-on-write)
