@@ -8,7 +8,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libfa.so")
 
 (FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_MISALIGNED, FA_ERR_LAUNCH, FA_ERR_TIMEOUT,
- FA_ERR_SCRATCH_LIMIT) = range(7)
+ FA_ERR_SCRATCH_LIMIT, FA_ERR_OUT_OF_PAGES) = range(8)
 FA_BWD_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 FA_DEVERR_SELFTEST_CODE = 0x10FF
 FA_OPT_RESCALE_TAU, FA_OPT_POLY_EXP, FA_OPT_WAIT_TIMEOUT_MS = 1, 2, 3
@@ -36,6 +36,16 @@ SIGNATURES = {
     "fa_bwd_masked_varlen": (_I, [_P] * 12 + [_I] * 10 + [_F, _P]),
     "fa_fp8_quantize": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "fa_fwd_fp8": (_I, [_P] * 8 + [_I] * 9 + [_F, _P]),
+    "fa_pool_create": (_P, [_I, _I, _I, _I]),
+    "fa_pool_destroy": (None, [_P]),
+    "fa_pool_free_pages": (_I, [_P]),
+    "fa_pool_refcount": (_I, [_P, _I]),
+    "fa_pool_add_seq": (_I, [_P, ctypes.POINTER(_I)]),
+    "fa_pool_fork": (_I, [_P, _I, ctypes.POINTER(_I)]),
+    "fa_pool_release": (_I, [_P, _I]),
+    "fa_pool_reserve_append": (_I, [_P, _P, _I, _P, _P, _P]),
+    "fa_pool_export": (_I, [_P, _P, _P]),
+    "fa_paged_append": (_I, [_P] * 7 + [_I] * 5 + [_P]),
     "fa_decode_workspace_bytes": (_S, [_I, _I, _I, _I]),
     "fa_decode_num_splits": (_I, [_I, _I, _I, _I]),
     "fa_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _F, _P]),

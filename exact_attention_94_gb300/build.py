@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfa.so")
-SOURCES = ["api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_decode.cu", "fa_fp8.cu"]
+SOURCES = ["api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_decode.cu", "fa_fp8.cu", "page_pool.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I", os.path.join(HERE, "..", "include")]
 
@@ -53,7 +53,7 @@ def build(verbose: bool = False, force: bool = False) -> str:
     objs = []
     for name in SOURCES:
         src = os.path.join(CSRC, name)
-        obj = os.path.join(BUILD, name.replace(".cu", ".o"))
+        obj = os.path.join(BUILD, os.path.splitext(name)[0] + ".o")
         objs.append(obj)
         if force or _stale(obj, _deps(src)):
             jobs.append([nvcc, *ARCH, *FLAGS, "-c", src, "-o", obj])

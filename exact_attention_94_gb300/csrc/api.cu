@@ -111,6 +111,7 @@ const char* fa_status_string(fa_status s) {
     case FA_ERR_LAUNCH: return "FA_ERR_LAUNCH";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
     case FA_ERR_SCRATCH_LIMIT: return "FA_ERR_SCRATCH_LIMIT";
+    case FA_ERR_OUT_OF_PAGES: return "FA_ERR_OUT_OF_PAGES";
   }
   return "FA_ERR_UNKNOWN";
 }
@@ -504,6 +505,23 @@ fa_status fa_fwd_fp8(const void* q_codes, const void* k_codes, const void* vt_co
   p.err = g_err_ptr;
   p.timeout_ns = g_opt.timeout_ns;
   cudaError_t e = launch_fwd_fp8(tq, tk, tvt, p, mask_kind(wl, wr), g_opt.poly, B * Hq, (cudaStream_t)stream);
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+fa_status fa_paged_append(const void* k_new, const void* v_new, void* k_pages, void* v_pages, const int* page,
+                          const int* slot, const int* copy_src, int n, int Hkv, int d, int page_size, int num_pages,
+                          fa_stream_t stream) {
+  if (n < 0 || Hkv < 1 || page_size < 1 || num_pages < 1) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (n == 0) return FA_OK;
+  if (!k_new || !v_new || !k_pages || !v_pages || !page || !slot || !copy_src) return FA_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pages) || !aligned16(v_pages)) return FA_ERR_MISALIGNED;
+  if (((reinterpret_cast<uintptr_t>(page) | reinterpret_cast<uintptr_t>(slot) |
+        reinterpret_cast<uintptr_t>(copy_src)) & 3u) != 0)
+    return FA_ERR_MISALIGNED;
+  if (!ensure_init()) return FA_ERR_LAUNCH;
+  cudaError_t e = launch_paged_append(k_new, v_new, k_pages, v_pages, page, slot, copy_src, n, Hkv, d, page_size,
+                                      num_pages, g_err_ptr, (cudaStream_t)stream);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

@@ -313,4 +313,53 @@ cudaError_t launch_decode(const DecodeParams& p, int D, void* o, float* lse, cud
   return cudaErrorInvalidValue;
 }
 
+// ---------------------------------------------------------------- paged cache: append
+//
+// One CTA per appended token: copy page copy_src -> page first when the
+// token's sequence shared a partly filled last page, then write the token's
+// K and V rows into its slot.  Sequences that still share a page all sit at
+// the same length, so a copy that overlaps another holder's in-place write
+// only reads the slot this CTA overwrites next.
+__global__ void __launch_bounds__(256) fa_paged_append_kernel(const uint4* __restrict__ k_new,
+                                                              const uint4* __restrict__ v_new, uint4* k_pages,
+                                                              uint4* v_pages, const int* __restrict__ page,
+                                                              const int* __restrict__ slot,
+                                                              const int* __restrict__ copy_src, int row_vec,
+                                                              int page_size, int num_pages, unsigned* err) {
+  const int i = blockIdx.x;
+  const int pg = page[i], sl = slot[i], src = copy_src[i];
+  if (pg < 0 || pg >= num_pages || sl < 0 || sl >= page_size || src >= num_pages) {
+    if (threadIdx.x == 0) atomicCAS(err, 0u, FA_DEVERR_BAD_PAGE);
+    return;
+  }
+  const size_t page_vec = (size_t)page_size * row_vec;  // 16-byte vectors per page
+  if (src >= 0) {
+    const uint4* ks = k_pages + (size_t)src * page_vec;
+    const uint4* vs = v_pages + (size_t)src * page_vec;
+    uint4* kd = k_pages + (size_t)pg * page_vec;
+    uint4* vd = v_pages + (size_t)pg * page_vec;
+    for (size_t t = threadIdx.x; t < page_vec; t += blockDim.x) {
+      kd[t] = ks[t];
+      vd[t] = vs[t];
+    }
+    __syncthreads();
+  }
+  uint4* kd = k_pages + (size_t)pg * page_vec + (size_t)sl * row_vec;
+  uint4* vd = v_pages + (size_t)pg * page_vec + (size_t)sl * row_vec;
+  for (int t = threadIdx.x; t < row_vec; t += blockDim.x) {
+    kd[t] = k_new[(size_t)i * row_vec + t];
+    vd[t] = v_new[(size_t)i * row_vec + t];
+  }
+}
+
+cudaError_t launch_paged_append(const void* k_new, const void* v_new, void* k_pages, void* v_pages, const int* page,
+                                const int* slot, const int* copy_src, int n, int Hkv, int d, int page_size,
+                                int num_pages, unsigned* err, cudaStream_t stream) {
+  const int row_vec = Hkv * d / 8;  // bf16 x 8 per vector
+  fa_paged_append_kernel<<<n, 256, 0, stream>>>(static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
+                                                static_cast<uint4*>(k_pages), static_cast<uint4*>(v_pages), page, slot,
+                                                copy_src, row_vec, page_size, num_pages, err);
+  return cudaGetLastError();
+}
+
 }  // namespace fa

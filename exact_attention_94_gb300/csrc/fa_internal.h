@@ -140,6 +140,11 @@ struct DecodeParams {
   unsigned long long timeout_ns;
 };
 
+// Paged cache appends: n CTAs, one per token (see fa_paged_append in fa.h).
+cudaError_t launch_paged_append(const void* k_new, const void* v_new, void* k_pages, void* v_pages, const int* page,
+                                const int* slot, const int* copy_src, int n, int Hkv, int d, int page_size,
+                                int num_pages, unsigned* err, cudaStream_t stream);
+
 int decode_stages(int G, int D);
 size_t decode_smem_bytes(int G, int D);
 cudaError_t launch_decode(const DecodeParams& p, int D, void* o, float* lse, cudaStream_t stream);

@@ -429,3 +429,80 @@ def fwd_fp8(q, k, v, signs=None, causal: bool = False, window: Optional[Tuple[in
     vc, vs = fp8_quantize(v, None, transpose=True, stream=stream)
     return fwd_fp8_codes(qc, kc, vc, qs, ks, vs, causal=causal, window=window, rotated=signs is not None,
                          scale=scale, stream=stream)
+
+
+# ---------------------------------------------------------------- paged cache: write side
+
+class PagePool:
+    """Host page allocator of the C library (block tables, free list,
+    reference counts); see fa_pool_* in fa.h.  Pages themselves are device
+    tensors [num_pages, page_size, Hkv, d] that the caller owns."""
+
+    def __init__(self, num_pages: int, page_size: int, max_seqs: int, max_blocks: int):
+        self._lib = lib()
+        self.handle = self._lib.fa_pool_create(num_pages, page_size, max_seqs, max_blocks)
+        if not self.handle:
+            raise _lib.FaError(_lib.FA_ERR_INVALID_ARG, "fa_pool_create")
+        self.num_pages, self.page_size, self.max_seqs, self.max_blocks = num_pages, page_size, max_seqs, max_blocks
+
+    def close(self):
+        if self.handle:
+            self._lib.fa_pool_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        self.close()
+
+    def free_pages(self) -> int:
+        return self._lib.fa_pool_free_pages(self.handle)
+
+    def refcount(self, page: int) -> int:
+        return self._lib.fa_pool_refcount(self.handle, page)
+
+    def add_seq(self) -> int:
+        s = ctypes.c_int(-1)
+        _lib.check(self._lib.fa_pool_add_seq(self.handle, ctypes.byref(s)), "fa_pool_add_seq")
+        return s.value
+
+    def fork(self, parent: int) -> int:
+        s = ctypes.c_int(-1)
+        _lib.check(self._lib.fa_pool_fork(self.handle, parent, ctypes.byref(s)), "fa_pool_fork")
+        return s.value
+
+    def release(self, seq: int) -> None:
+        _lib.check(self._lib.fa_pool_release(self.handle, seq), "fa_pool_release")
+
+    def reserve_append(self, seqs):
+        """Next token of each sequence: int32 host tensors (page, slot, copy_src)."""
+        seqs_t = torch.as_tensor(list(seqs), dtype=torch.int32)
+        n = seqs_t.numel()
+        page, slot, src = (torch.empty(n, dtype=torch.int32) for _ in range(3))
+        _lib.check(self._lib.fa_pool_reserve_append(self.handle, _ptr(seqs_t), n, _ptr(page), _ptr(slot), _ptr(src)),
+                   "fa_pool_reserve_append")
+        return page, slot, src
+
+    def export(self):
+        """(block_table int32 [max_seqs, max_blocks], seq_lens int32 [max_seqs]), host."""
+        table = torch.empty((self.max_seqs, self.max_blocks), dtype=torch.int32)
+        lens = torch.empty(self.max_seqs, dtype=torch.int32)
+        _lib.check(self._lib.fa_pool_export(self.handle, _ptr(table), _ptr(lens)), "fa_pool_export")
+        return table, lens
+
+
+def paged_append(k_new, v_new, k_pages, v_pages, page, slot, copy_src, stream=None):
+    """Copies shared pages where copy_src >= 0, then writes each token's K, V
+    rows ([n, Hkv, d] bf16) into (page, slot); index tensors int32 on the device."""
+    _check_bf16("k_new", k_new)
+    n, Hkv, d = k_new.shape
+    _check_bf16("v_new", v_new, k_new.shape)
+    _check_bf16("k_pages", k_pages)
+    num_pages, P = k_pages.shape[0], k_pages.shape[1]
+    if tuple(k_pages.shape) != (num_pages, P, Hkv, d):
+        raise ValueError("k_pages must be [num_pages, page_size, Hkv, d]")
+    _check_bf16("v_pages", v_pages, k_pages.shape)
+    for name, t in (("page", page), ("slot", slot), ("copy_src", copy_src)):
+        if t.dtype != torch.int32 or not t.is_cuda or t.numel() != n or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor of {n} entries")
+    st = lib().fa_paged_append(_ptr(k_new), _ptr(v_new), _ptr(k_pages), _ptr(v_pages), _ptr(page), _ptr(slot),
+                               _ptr(copy_src), n, Hkv, d, P, num_pages, _stream(stream))
+    _lib.check(st, "fa_paged_append")

@@ -58,7 +58,8 @@ typedef enum {
   FA_ERR_MISALIGNED = 3,  /* a device pointer not 16-byte aligned */
   FA_ERR_LAUNCH = 4,      /* the CUDA runtime refused a launch */
   FA_ERR_TIMEOUT = 5,     /* a bounded wait inside a kernel ran out */
-  FA_ERR_SCRATCH_LIMIT = 6 /* fa_bwd_noalloc: the problem needs more than its built-in scratch */
+  FA_ERR_SCRATCH_LIMIT = 6, /* fa_bwd_noalloc: the problem needs more than its built-in scratch */
+  FA_ERR_OUT_OF_PAGES = 7   /* page pool: no free page (or sequence slot) for the request; nothing changed */
 } fa_status;
 
 /* Human-readable name of a status code (static storage). */
@@ -245,6 +246,60 @@ fa_status fa_fp8_quantize(const void* x, const signed char* signs, void* codes, 
 fa_status fa_fwd_fp8(const void* q_codes, const void* k_codes, const void* vt_codes, const float* q_scale,
                      const float* k_scale, const float* v_scale, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
                      int Nk, int d, int window_left, int window_right, int rotated, float scale, fa_stream_t stream);
+
+/*
+ * Paged KV cache, write side ("efficient-attention/flash-2-3", section "Paged
+ * KV caches, a preview of serving"): the cache is a pool of pages of
+ * page_size tokens; each sequence's block table maps its logical blocks to
+ * pages; a page is taken from the free list only when the sequence's last
+ * page fills; sequences that share a prompt share its pages and copy one only
+ * when they would write to it.  The pool object is host memory and does no
+ * device work; fa_paged_append moves the data; fa_decode_paged reads it.
+ * Policies: the free list is a stack (page 0 is taken first, a released page
+ * is the next one taken); a new sequence takes the smallest free slot.
+ * The functions are not thread-safe on one pool.
+ */
+typedef struct fa_page_pool fa_page_pool;
+
+/* A pool of num_pages pages for up to max_seqs sequences of up to max_blocks
+ * blocks each; NULL for a size below 1 or when host memory runs out. */
+fa_page_pool* fa_pool_create(int num_pages, int page_size, int max_seqs, int max_blocks);
+void fa_pool_destroy(fa_page_pool* pool);
+int fa_pool_free_pages(const fa_page_pool* pool);          /* -1 for NULL */
+int fa_pool_refcount(const fa_page_pool* pool, int page);  /* tables holding the page; -1 if invalid */
+
+/* A new, empty sequence in the smallest free slot (*seq); FA_ERR_OUT_OF_PAGES when none is free. */
+fa_status fa_pool_add_seq(fa_page_pool* pool, int* seq);
+/* A new sequence (*child) sharing every page of parent, e.g. a common prompt. */
+fa_status fa_pool_fork(fa_page_pool* pool, int parent, int* child);
+/* Drops a sequence; pages no table holds any more return to the free list. */
+fa_status fa_pool_release(fa_page_pool* pool, int seq);
+
+/*
+ * Reserves the next token of each of n distinct live sequences seqs[0..n-1]
+ * (host arrays): page[i], slot[i] receive where the token goes and
+ * copy_src[i] the page to copy into page[i] first (-1 for none: only a shared,
+ * partly filled last page is copied).  All or nothing: FA_ERR_OUT_OF_PAGES if
+ * the free list cannot cover the batch, FA_ERR_INVALID_ARG for a bad or
+ * repeated sequence or a full block table, and then nothing changes.
+ */
+fa_status fa_pool_reserve_append(fa_page_pool* pool, const int* seqs, int n, int* page, int* slot, int* copy_src);
+
+/* Block tables [max_seqs, max_blocks] (unused entries 0) and lengths [max_seqs], host int32. */
+fa_status fa_pool_export(const fa_page_pool* pool, int* block_table, int* seq_lens);
+
+/*
+ * Device side of n appends: for entry i, copies page copy_src[i] into page[i]
+ * when copy_src[i] >= 0, then writes token i into slot slot[i] of page[i].
+ *   k_new, v_new     : [n, Hkv, d] bf16, device
+ *   k_pages, v_pages : [num_pages, page_size, Hkv, d] bf16, device, updated
+ *   page, slot, copy_src : int32 [n], DEVICE memory (from fa_pool_reserve_append)
+ * Entries naming a page outside the pool are skipped and reported by
+ * fa_device_error (FA_ERR_INVALID_ARG).  d = 64 or 128.
+ */
+fa_status fa_paged_append(const void* k_new, const void* v_new, void* k_pages, void* v_pages, const int* page,
+                          const int* slot, const int* copy_src, int n, int Hkv, int d, int page_size, int num_pages,
+                          fa_stream_t stream);
 
 /*
  * Size of the built-in scratch of fa_bwd_noalloc: 32 MiB of device memory,
