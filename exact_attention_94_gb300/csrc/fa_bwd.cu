@@ -616,8 +616,8 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
   auto row_base_of = [&](int hq) { return (size_t)(b_coord * p.H + hq) * p.n_rows + seq_start; };
 
   enum { KV_FULL = 0, Q_FULL = 1, STAGE_EMPTY = Q_FULL + NST, S_FULL = STAGE_EMPTY + NST, DP_FULL = S_FULL + 1,
-         P_READY = DP_FULL + 1,
-         DQ_FULL = P_READY + 4, DQ_EMPTY, DKV_FINAL, DRAIN, NBARS };
+         P_READY = DP_FULL + 1, DS_READY = P_READY + 4,
+         DQ_FULL = DS_READY + 4, DQ_EMPTY, DKV_FINAL, DRAIN, NBARS };
   const uint32_t bar0 = base + L::kBar;
   auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + L::kBar + 8 * NBARS);
@@ -633,7 +633,10 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
     }
     mbar_init(BAR(S_FULL), 1);
     mbar_init(BAR(DP_FULL), 1);
-    for (int i = 0; i < 4; ++i) mbar_init(BAR(P_READY + i), 128);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(BAR(P_READY + i), 128);
+      mbar_init(BAR(DS_READY + i), 128);
+    }
     mbar_init(BAR(DQ_FULL), 1);
     mbar_init(BAR(DQ_EMPTY), 256);
     mbar_init(BAR(DKV_FINAL), 1);
@@ -726,19 +729,34 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
         }
         mma_commit(BAR(DP_FULL));
         // dV += P^T dO_i and dK += dS^T Q_i, one 32-query quarter at a time as the groups hand them over:
-        // quarter i = group (i & 1), half (i >> 1); queries qb .. qb+31 with qb = 64*group + 32*half
+        // quarter i = group (i & 1), half (i >> 1); queries qb .. qb+31 with qb = 64*group + 32*half.
+        // P^T of a quarter arrives before its dS^T (P needs S^T only, dS also dP^T), so each half's
+        // dV products run while the groups still compute that half's dS.
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int g = i & 1, r = i >> 1;
-          const int qb = 64 * g + 32 * r;
-          if (!(ok = mbar_wait(BAR(P_READY + i), n & 1, w, 55))) break;
-          tc_fence_after();
+        for (int r = 0; r < 2 && ok; ++r) {
 #pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {
-            const uint32_t acc = (n > 0 || i > 0 || kk > 0) ? 1u : 0u;
-            const uint32_t rows = (uint32_t)(qb / 16 + kk) * 2048;  // 16 query rows of Q_i / dO_i
-            mma_ts(tDV, tS + 64 * g + 16 * r + 8 * kk, desc_add(do_mn, rows), IDESC_KV, acc);
-            mma_ss(tDK, desc_add(dDS_k, g * CHUNK + (2 * r + kk) * 32), desc_add(q_mn, rows), IDESC_KV, acc);
+          for (int g = 0; g < 2; ++g) {
+            const int i = 2 * r + g, qb = 64 * g + 32 * r;
+            if (!(ok = mbar_wait(BAR(P_READY + i), n & 1, w, 55))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+              const uint32_t acc = (n > 0 || i > 0 || kk > 0) ? 1u : 0u;
+              const uint32_t rows = (uint32_t)(qb / 16 + kk) * 2048;  // 16 query rows of dO_i
+              mma_ts(tDV, tS + 64 * g + 16 * r + 8 * kk, desc_add(do_mn, rows), IDESC_KV, acc);
+            }
+          }
+#pragma unroll
+          for (int g = 0; g < 2 && ok; ++g) {
+            const int i = 2 * r + g, qb = 64 * g + 32 * r;
+            if (!(ok = mbar_wait(BAR(DS_READY + i), n & 1, w, 56))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+              const uint32_t acc = (n > 0 || i > 0 || kk > 0) ? 1u : 0u;
+              const uint32_t rows = (uint32_t)(qb / 16 + kk) * 2048;  // 16 query rows of Q_i
+              mma_ss(tDK, desc_add(dDS_k, g * CHUNK + (2 * r + kk) * 32), desc_add(q_mn, rows), IDESC_KV, acc);
+            }
           }
         }
         if (!ok) break;
@@ -803,66 +821,75 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
       const float sl2 = p.scale_log2, scale = p.scale;
       uint8_t* ds_row = sbase + L::kDS + g * CHUNK + kr * 128;
 #pragma unroll 1
-      for (int r = 0; r < 2; ++r) {  // quarter: 32 queries, handled as two runs of 16
+      for (int r = 0; r < 2; ++r) {  // quarter: 32 queries
+        const uint32_t col = 64u * g + 32u * r;  // S^T / dP^T columns of the quarter
+        // ---- P (needs S^T only): handed to the dV products before dS exists
+        uint32_t sr[32];
+        tmem_ld16(tmem + lane_off + col, sr);
+        tmem_ld16(tmem + lane_off + col + 16, sr + 16);
+        tmem_ld_wait();
+        const float4* nl4 = reinterpret_cast<const float4*>(my_lse2 + 32 * r);  // -lse2
+        // P = 2^(s * scale * log2 e - lse2)
+        float pv[32];
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const uint32_t col = 64u * g + 32u * r + 16u * hh;  // S^T / dP^T columns of this run
-          uint32_t sr[16], dr[16];
-          tmem_ld16(tmem + lane_off + col, sr);
-          if (r == 0 && hh == 0) {  // dP^T lands after S^T
-            ok = mbar_wait(BAR(DP_FULL), n & 1, w, 61);
-            if (!__all_sync(0xffffffffu, ok)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-          }
-          tmem_ld16(tmem + lane_off + 128 + col, dr);
-          tmem_ld_wait();
-          const float4* nl4 = reinterpret_cast<const float4*>(my_lse2 + 32 * r + 16 * hh);  // -lse2
-          const float4* nd4 = reinterpret_cast<const float4*>(my_dsum + 32 * r + 16 * hh);  // -scale * D
-          // P = 2^(s * scale * log2 e - lse2)
-          float pv[16];
+        for (int e = 0; e < 32; ++e) pv[e] = __uint_as_float(sr[e]);
 #pragma unroll
-          for (int e4 = 0; e4 < 4; ++e4) {
-            const float4 nl = nl4[e4];
-            pv[4 * e4 + 0] = ex2_sfu(fmaf(__uint_as_float(sr[4 * e4 + 0]), sl2, nl.x));
-            pv[4 * e4 + 1] = ex2_sfu(fmaf(__uint_as_float(sr[4 * e4 + 1]), sl2, nl.y));
-            pv[4 * e4 + 2] = ex2_sfu(fmaf(__uint_as_float(sr[4 * e4 + 2]), sl2, nl.z));
-            pv[4 * e4 + 3] = ex2_sfu(fmaf(__uint_as_float(sr[4 * e4 + 3]), sl2, nl.w));
-          }
-          if (masked || (tail_rows && !row_ok)) {  // masks in a separate, warp-uniform pass
-            const int q16 = qs + 32 * r + 16 * hh;
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              if (!row_ok || (masked && (q16 + e < ma || q16 + e > mb))) pv[e] = 0.f;
-          }
-          // dS = P * (scale * dP - scale * D)
-          uint32_t pp[8], dd[8];
-#pragma unroll
-          for (int e4 = 0; e4 < 4; ++e4) {
-            const float4 nd = nd4[e4];
-            const float g0 = pv[4 * e4 + 0] * fmaf(__uint_as_float(dr[4 * e4 + 0]), scale, nd.x);
-            const float g1 = pv[4 * e4 + 1] * fmaf(__uint_as_float(dr[4 * e4 + 1]), scale, nd.y);
-            const float g2 = pv[4 * e4 + 2] * fmaf(__uint_as_float(dr[4 * e4 + 2]), scale, nd.z);
-            const float g3 = pv[4 * e4 + 3] * fmaf(__uint_as_float(dr[4 * e4 + 3]), scale, nd.w);
-            pp[2 * e4] = pack_bf16x2(pv[4 * e4 + 0], pv[4 * e4 + 1]);
-            pp[2 * e4 + 1] = pack_bf16x2(pv[4 * e4 + 2], pv[4 * e4 + 3]);
-            dd[2 * e4] = pack_bf16x2(g0, g1);
-            dd[2 * e4 + 1] = pack_bf16x2(g2, g3);
-          }
-          // P^T over this group's already-read S^T columns: query q at column 64*(q/64) + (q%64)/2
-          tmem_st8(tmem + lane_off + 64u * g + 16u * r + 8u * hh, pp);
-          // dS^T row kr, 16 queries = two 16-byte units of the 128-byte swizzled row
-          const int unit = 4 * r + 2 * hh;
-          *reinterpret_cast<uint4*>(ds_row + ((unit ^ swz) << 4)) = make_uint4(dd[0], dd[1], dd[2], dd[3]);
-          *reinterpret_cast<uint4*>(ds_row + (((unit + 1) ^ swz) << 4)) = make_uint4(dd[4], dd[5], dd[6], dd[7]);
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 nl = nl4[e4];
+          pv[4 * e4 + 0] = ex2_sfu(fmaf(pv[4 * e4 + 0], sl2, nl.x));
+          pv[4 * e4 + 1] = ex2_sfu(fmaf(pv[4 * e4 + 1], sl2, nl.y));
+          pv[4 * e4 + 2] = ex2_sfu(fmaf(pv[4 * e4 + 2], sl2, nl.z));
+          pv[4 * e4 + 3] = ex2_sfu(fmaf(pv[4 * e4 + 3], sl2, nl.w));
         }
-        if (!ok) break;
+        if (masked || (tail_rows && !row_ok)) {  // masks in a separate, warp-uniform pass
+          const int q32 = qs + 32 * r;
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (!row_ok || (masked && (q32 + e < ma || q32 + e > mb))) pv[e] = 0.f;
+        }
+        {
+          uint32_t pp[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) pp[e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
+          // P^T over this group's already-read S^T columns: query q at column 64*(q/64) + (q%64)/2
+          tmem_st8(tmem + lane_off + 64u * g + 16u * r, pp);
+          tmem_st8(tmem + lane_off + 64u * g + 16u * r + 8u, pp + 8);
+        }
         tmem_st_wait();
-        fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(BAR(P_READY + 2 * r + g));
+        // ---- dS = P * (scale * dP - scale * D): needs dP^T, which lands after S^T
+        if (r == 0) {
+          ok = mbar_wait(BAR(DP_FULL), n & 1, w, 61);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        uint32_t dr[32];
+        tmem_ld16(tmem + lane_off + 128 + col, dr);
+        tmem_ld16(tmem + lane_off + 128 + col + 16, dr + 16);
+        tmem_ld_wait();
+        const float4* nd4 = reinterpret_cast<const float4*>(my_dsum + 32 * r);  // -scale * D
+        uint32_t dd[16];
+#pragma unroll
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 nd = nd4[e4];
+          const float g0 = pv[4 * e4 + 0] * fmaf(__uint_as_float(dr[4 * e4 + 0]), scale, nd.x);
+          const float g1 = pv[4 * e4 + 1] * fmaf(__uint_as_float(dr[4 * e4 + 1]), scale, nd.y);
+          const float g2 = pv[4 * e4 + 2] * fmaf(__uint_as_float(dr[4 * e4 + 2]), scale, nd.z);
+          const float g3 = pv[4 * e4 + 3] * fmaf(__uint_as_float(dr[4 * e4 + 3]), scale, nd.w);
+          dd[2 * e4] = pack_bf16x2(g0, g1);
+          dd[2 * e4 + 1] = pack_bf16x2(g2, g3);
+        }
+        // dS^T row kr, 32 queries = four 16-byte units of the 128-byte swizzled row
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          *reinterpret_cast<uint4*>(ds_row + (((4 * r + u) ^ swz) << 4)) =
+              make_uint4(dd[4 * u], dd[4 * u + 1], dd[4 * u + 2], dd[4 * u + 3]);
+        fence_proxy_async_smem();
+        mbar_arrive(BAR(DS_READY + 2 * r + g));
       }
     }
     // ------------------------------------------------------------ epilogue: group 0 writes dV, group 1 dK
