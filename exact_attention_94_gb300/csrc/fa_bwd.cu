@@ -17,15 +17,9 @@
 //            dQ_i  = dS K_j  -> added into dQacc with vector atomics
 //   post:  dQ = bf16(dQacc)
 //
-// The fp32 dQ accumulator is laid out [B*H][d/4][rows][4]: a warp's 32
-// threads (32 consecutive query rows) add one 4-float group each, so every
-// warp-wide atomic covers 512 contiguous bytes.
-//
-// CTA roles (384 threads): warp 0 TMA producer, warp 1 TMEM owner and MMA
-// issuer, warps 4-7 recompute P and dS (thread = key row = TMEM lane),
-// warps 8-11 drain dQ tiles from TMEM into the accumulator (thread = query
-// row).  TMEM: S^T/P^T [0,128), dP^T/dQ [128,256), dV [256,256+d),
-// dK [256+d,256+2d).
+// The fp32 dQ accumulator is laid out per d (see acc_f4_index) so that a
+// warp's atomics always cover contiguous bytes.  The main kernel is described
+// above fa_bwd_main_ov_kernel.
 #include "fa_internal.h"
 #include "ptx.cuh"
 
@@ -36,21 +30,7 @@ namespace fa {
 
 namespace {
 
-constexpr int kBwdThreads = 384;
 constexpr int kBwdHeadGroup = 8;
-
-template <int D>
-struct BwdLayout {
-  static constexpr uint32_t kTile = 128u * D * 2u;  // one 128-row bf16 tile
-  static constexpr uint32_t kChunk = 128u * 128u;   // 128 rows x 128 bytes
-  static constexpr uint32_t kK = 0;
-  static constexpr uint32_t kV = kTile;
-  static constexpr uint32_t kStage0 = 2 * kTile;     // stage s: Q_i then dO_i
-  static constexpr uint32_t kStageBytes = 2 * kTile;
-  static constexpr uint32_t kDS = kStage0 + 2 * kStageBytes;  // 128 x 128 bf16, two 64-column chunks
-  static constexpr uint32_t kBar = kDS + 2 * kChunk;
-  static constexpr uint32_t kBytes = kBar + 128 + 1024 + 1024;  // barriers, lse2/D rows, alignment slack
-};
 
 }  // namespace
 
@@ -209,359 +189,35 @@ __device__ void bwd_zero_dkdv(const BwdParams& p, const BwdItem& it, int Hkv, in
 
 // ---------------------------------------------------------------- main
 
-template <int D, int MASK>
-__global__ void __launch_bounds__(kBwdThreads, 1)
-    fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                       const BwdParams p) {
-  using L = BwdLayout<D>;
-  constexpr int CH = D / 64;
-  constexpr uint32_t TILE = L::kTile;
-  constexpr uint32_t CHUNK = L::kChunk;
-
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* sbase = smem_raw + (base - raw);
-
-  const int warp = warp_id();
-  const int lane = lane_id();
-
-  // ---------------------------------------------------------------- work item
-  // one CTA per (batch, K/V head, key block); with grouped-query attention it
-  // walks the query blocks of every query head that shares this K/V head
-  const int Hkv = p.H / p.kv_group;
-  const int bh = (int)(blockIdx.z * gridDim.x + blockIdx.x);
-  if (bh >= p.B * Hkv) return;
-  const int b = bh / Hkv;
-  const int h_kv = bh % Hkv;
-  const int jb = (int)blockIdx.y;  // key block; ascending = heaviest first when causal
-  const int k0 = jb * 128;
-  const BwdItem it = bwd_item<MASK>(p, b, k0);
-  if (it.bad) {
-    if (threadIdx.x == 0 && p.err != nullptr) atomicCAS(p.err, 0u, FA_DEVERR_BAD_SEQLEN);
-    return;
-  }
-  const int seq_start = it.seq_start, seq_len = it.seq_len, kv_start = it.kv_start, b_coord = it.b_coord;
-  if (k0 >= it.kv_len) return;
-  const int q_begin = it.q_lo;
-  const int n_q = it.q_hi > it.q_lo ? (it.q_hi - it.q_lo + 127) / 128 : 0;  // query blocks per query head
-  if (n_q == 0) {  // uniform for the CTA, before any shared state exists
-    bwd_zero_dkdv<D>(p, it, Hkv, h_kv, k0);
-    return;
-  }
-  const int n_steps = p.kv_group * n_q;   // step n: query head hq(n), rows q_begin + 128 (n % n_q) + [0, 128)
-  auto hq_of = [&](int n) { return h_kv * p.kv_group + n / n_q; };
-  auto row_base_of = [&](int hq) { return (size_t)(b_coord * p.H + hq) * p.n_rows + seq_start; };  // lse2 / dsum / acc
-
-  // ---------------------------------------------------------------- barriers
-  enum { KV_FULL = 0, Q_FULL = 1, STAGE_EMPTY = 3, S_FULL = 5, DP_FULL, P_READY, DQ_FULL, DQ_EMPTY, DS_EMPTY,
-         DKV_FINAL, DRAIN, NBARS };
-  const uint32_t bar0 = base + L::kBar;
-  auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + L::kBar + 8 * NBARS);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* s_lse2 = reinterpret_cast<float*>(sbase + L::kBar + 128);  // 128 floats
-  float* s_dsum = s_lse2 + 128;                                     // 128 floats
-
-  if (threadIdx.x == 0) {
-    mbar_init(BAR(KV_FULL), 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(BAR(Q_FULL + s), 1);
-      mbar_init(BAR(STAGE_EMPTY + s), 1);
-    }
-    mbar_init(BAR(S_FULL), 1);
-    mbar_init(BAR(DP_FULL), 1);
-    mbar_init(BAR(P_READY), 128);
-    mbar_init(BAR(DQ_FULL), 1);
-    mbar_init(BAR(DQ_EMPTY), 128);
-    mbar_init(BAR(DS_EMPTY), 1);
-    mbar_init(BAR(DKV_FINAL), 1);
-    mbar_init(BAR(DRAIN), 1);
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const WaitCtx w{abort_flag, p.timeout_ns, p.err};
-
-  const uint32_t sK = base + L::kK, sV = base + L::kV, sDS = base + L::kDS;
-  auto stage_q = [&](int st) -> uint32_t { return base + L::kStage0 + (uint32_t)st * L::kStageBytes; };
-
-  if (warp == 0) {
-    // ============================================================ TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      tma_prefetch_desc(&tm_do);
-      mbar_arrive_expect_tx(BAR(KV_FULL), 2 * TILE);
-      for (int c = 0; c < CH; ++c) {
-        tma_load_4d(sK + c * CHUNK, &tm_k, BAR(KV_FULL), c * 64, kv_start + k0, h_kv, b_coord);
-        tma_load_4d(sV + c * CHUNK, &tm_v, BAR(KV_FULL), c * 64, kv_start + k0, h_kv, b_coord);
-      }
-      bool ok = true;
-      for (int n = 0; n < n_steps && ok; ++n) {
-        const int st = n & 1;
-        const int row = seq_start + q_begin + (n % n_q) * 128;
-        const int hq = hq_of(n);
-        if (n >= 2 && !(ok = mbar_wait(BAR(STAGE_EMPTY + st), ((n >> 1) - 1) & 1, w, 21))) break;
-        mbar_arrive_expect_tx(BAR(Q_FULL + st), 2 * TILE);
-        const uint32_t qa = stage_q(st);
-        for (int c = 0; c < CH; ++c) {
-          tma_load_4d(qa + c * CHUNK, &tm_q, BAR(Q_FULL + st), c * 64, row, hq, b_coord);
-          tma_load_4d(qa + TILE + c * CHUNK, &tm_do, BAR(Q_FULL + st), c * 64, row, hq, b_coord);
-        }
-      }
-      if (!ok) {
-        const uint64_t t0 = globaltimer_ns();
-        while (globaltimer_ns() - t0 < 200000ull) {
-        }
-      }
-    }
-  } else if (warp == 1) {
-    // ============================================================ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t IDESC_ST = idesc_bf16(128, 128, false, false);  // S^T, dP^T
-      constexpr uint32_t IDESC_KV = idesc_bf16(128, D, false, true);     // dV, dK
-      constexpr uint32_t IDESC_Q = idesc_bf16(128, D, true, true);       // dQ
-      const uint32_t tS = tmem, tDP = tmem + 128, tDV = tmem + 256, tDK = tmem + 256 + D;
-      bool ok = mbar_wait(BAR(KV_FULL), 0, w, 22);
-      tc_fence_after();
-      for (int n = 0; n < n_steps && ok; ++n) {
-        const int st = n & 1;
-        const uint32_t qa = stage_q(st), da = qa + TILE;
-        if (!(ok = mbar_wait(BAR(Q_FULL + st), (n >> 1) & 1, w, 23))) break;
-        tc_fence_after();
-        // S^T = K_j Q_i^T   (M = keys, N = queries, K = d; both K-major)
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * CHUNK + (kk % 4) * 32;
-          mma_ss(tS, smem_desc_sw128(sK + off, 16, 1024), smem_desc_sw128(qa + off, 16, 1024), IDESC_ST, kk > 0);
-        }
-        mma_commit(BAR(S_FULL));
-        if (n > 0) {
-          if (!(ok = mbar_wait(BAR(DQ_EMPTY), (n - 1) & 1, w, 24))) break;
-          tc_fence_after();
-        }
-        // dP^T = V_j dO_i^T
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * CHUNK + (kk % 4) * 32;
-          mma_ss(tDP, smem_desc_sw128(sV + off, 16, 1024), smem_desc_sw128(da + off, 16, 1024), IDESC_ST, kk > 0);
-        }
-        mma_commit(BAR(DP_FULL));
-        if (!(ok = mbar_wait(BAR(P_READY), n & 1, w, 25))) break;
-        tc_fence_after();
-        // dV += P^T dO_i   (A = P^T from TMEM, B = dO_i MN-major; K = 128 queries)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tDV, tS + kk * 8, smem_desc_sw128(da + kk * 2048, CHUNK, 1024), IDESC_KV, (n > 0 || kk > 0) ? 1u : 0u);
-        // dK += dS^T Q_i   (A = dS^T K-major in shared memory, B = Q_i MN-major)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tDK, smem_desc_sw128(sDS + (kk / 4) * CHUNK + (kk % 4) * 32, 16, 1024),
-                 smem_desc_sw128(qa + kk * 2048, CHUNK, 1024), IDESC_KV, (n > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(BAR(STAGE_EMPTY + st));
-        // dQ_i = dS K_j   (M = queries: A = dS MN-major over the same buffer, B = K_j MN-major; K = 128 keys)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tDP, smem_desc_sw128(sDS + kk * 2048, CHUNK, 1024), smem_desc_sw128(sK + kk * 2048, CHUNK, 1024),
-                 IDESC_Q, kk > 0);
-        mma_commit(BAR(DQ_FULL));
-        mma_commit(BAR(DS_EMPTY));
-      }
-      if (ok) mma_commit(BAR(DKV_FINAL));
-      mma_commit(BAR(DRAIN));
-      const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(BAR(DRAIN), 0) && globaltimer_ns() - t0 < p.timeout_ns) {
-      }
-    }
-  } else if (warp >= 4 && warp < 8) {
-    // ============================================================ P and dS (thread = key row)
-    const int kw = warp & 3;
-    const int kr = kw * 32 + lane;
-    const int kg = k0 + kr;
-    const bool row_ok = kg < it.kv_len;
-    const int ma = mask_a<MASK>(p, it, kg), mb = mask_b<MASK>(p, it, kg);
-    const uint32_t lane_off = (uint32_t)(kw * 32) << 16;
-    const uint32_t tS = tmem + lane_off, tDP = tmem + lane_off + 128;
-    const float sl2 = p.scale_log2;
-    const float scale = p.scale;
-    const int swz = kr & 7;
-    uint8_t* ds_row = sbase + L::kDS + kr * 128;
-    bool ok = true;
-    // this thread's lse2 and D of the next query block, fetched one step ahead
-    // (invalid rows: lse2 = +inf, so P = 0)
-    auto fetch = [&](int n, float& l2, float& ds) {
-      const int qg = q_begin + (n % n_q) * 128 + kr;
-      const bool qv = n < n_steps && qg < seq_len;
-      const size_t rb = n < n_steps ? row_base_of(hq_of(n)) : 0;
-      l2 = qv ? p.lse2[rb + qg] : INFINITY;
-      ds = qv ? p.dsum[rb + qg] : 0.f;
-    };
-    float pf_l, pf_d;
-    fetch(0, pf_l, pf_d);
-    for (int n = 0; n < n_steps; ++n) {
-      const int q0 = q_begin + (n % n_q) * 128;
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      s_lse2[kr] = pf_l;
-      s_dsum[kr] = pf_d;
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      fetch(n + 1, pf_l, pf_d);
-      // After an abort the warp keeps taking part in the two named barriers of every
-      // step (so the other warps of the group never wait on it) and does nothing else.
-      if (!ok) continue;
-      ok = mbar_wait(BAR(S_FULL), n & 1, w, 26) && mbar_wait(BAR(DP_FULL), n & 1, w, 27) &&
-           (n == 0 || mbar_wait(BAR(DS_EMPTY), (n - 1) & 1, w, 28));
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        continue;
-      }
-      tc_fence_after();
-      const bool masked = mask_needed<MASK>(p, it, k0, q0, 128);
-#pragma unroll 2
-      for (int c = 0; c < 8; ++c) {
-        uint32_t sr[16], dr[16];
-        tmem_ld16(tS + 16 * c, sr);
-        tmem_ld16(tDP + 16 * c, dr);
-        tmem_ld_wait();
-        const float4* l4 = reinterpret_cast<const float4*>(s_lse2 + 16 * c);
-        const float4* d4 = reinterpret_cast<const float4*>(s_dsum + 16 * c);
-        float lv[16], dv[16];
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const float4 a = l4[g], bq = d4[g];
-          lv[4 * g] = a.x; lv[4 * g + 1] = a.y; lv[4 * g + 2] = a.z; lv[4 * g + 3] = a.w;
-          dv[4 * g] = bq.x; dv[4 * g + 1] = bq.y; dv[4 * g + 2] = bq.z; dv[4 * g + 3] = bq.w;
-        }
-        uint32_t pp[8], dd[8];
-#pragma unroll
-        for (int e = 0; e < 16; e += 2) {
-          float p0 = ex2_sfu(fmaf(__uint_as_float(sr[e]), sl2, -lv[e]));
-          float p1 = ex2_sfu(fmaf(__uint_as_float(sr[e + 1]), sl2, -lv[e + 1]));
-          if (!row_ok) {
-            p0 = 0.f;
-            p1 = 0.f;
-          }
-          if (masked) {
-            const int qg = q0 + 16 * c + e;
-            if (qg < ma || qg > mb) p0 = 0.f;
-            if (qg + 1 < ma || qg + 1 > mb) p1 = 0.f;
-          }
-          const float g0 = p0 * scale * (__uint_as_float(dr[e]) - dv[e]);
-          const float g1 = p1 * scale * (__uint_as_float(dr[e + 1]) - dv[e + 1]);
-          pp[e / 2] = pack_bf16x2(p0, p1);
-          dd[e / 2] = pack_bf16x2(g0, g1);
-        }
-        tmem_st8(tS + 8 * c, pp);  // P^T over already-consumed S^T columns
-        // dS^T row kr, queries 16c..16c+15: 128-byte swizzled K-major layout
-        const int unit = 2 * (c & 3);
-        uint8_t* chunk = ds_row + (c >> 2) * CHUNK;
-        *reinterpret_cast<uint4*>(chunk + ((unit ^ swz) << 4)) = make_uint4(dd[0], dd[1], dd[2], dd[3]);
-        *reinterpret_cast<uint4*>(chunk + (((unit + 1) ^ swz) << 4)) = make_uint4(dd[4], dd[5], dd[6], dd[7]);
-      }
-      tmem_st_wait();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(BAR(P_READY));
-    }
-    // ------------------------------------------------------------ dK, dV epilogue
-    if (ok) {
-      ok = mbar_wait(BAR(DKV_FINAL), 0, w, 29);
-      if (__all_sync(0xffffffffu, ok)) {
-        tc_fence_after();
-        const size_t grow = ((size_t)b_coord * p.n_rows_k + kv_start + kg) * Hkv + h_kv;
-        __nv_bfloat16* dv_row = reinterpret_cast<__nv_bfloat16*>(p.dv) + grow * D;
-        __nv_bfloat16* dk_row = reinterpret_cast<__nv_bfloat16*>(p.dk) + grow * D;
-#pragma unroll
-        for (int which = 0; which < 2; ++which) {
-          const uint32_t src = tmem + lane_off + 256 + (which ? (uint32_t)D : 0u);
-          __nv_bfloat16* dst = which ? dk_row : dv_row;
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(src + 32 * c, v);
-            tmem_ld_wait();
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-            if (row_ok) {
-              uint4* o4 = reinterpret_cast<uint4*>(dst + 32 * c);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) o4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-            }
-          }
-        }
-      }
-    }
-  } else if (warp >= 8) {
-    // ============================================================ dQ drain (thread = query row)
-    const int qw = warp & 3;
-    const int r = qw * 32 + lane;
-    const uint32_t tDQ = tmem + ((uint32_t)(qw * 32) << 16) + 128;
-    for (int n = 0; n < n_steps; ++n) {
-      float4* acc = reinterpret_cast<float4*>(p.dq_acc) + (size_t)(b_coord * p.H + hq_of(n)) * (D / 4) * p.n_rows;
-      const int qg = q_begin + (n % n_q) * 128 + r;
-      bool ok = mbar_wait(BAR(DQ_FULL), n & 1, w, 30);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      tc_fence_after();
-      uint32_t v[D];
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_ld32(tDQ + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(BAR(DQ_EMPTY));  // TMEM free for the next dP^T while the adds go out
-      if (qg < it.q_hi) {  // rows past q_hi see none of this block's keys: their share is zero
-        const size_t row = (size_t)seq_start + qg;
-#pragma unroll
-        for (int g = 0; g < D / 4; ++g)
-          atomicAdd(acc + (size_t)g * p.n_rows + row,
-                    make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
-                                __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3])));
-      }
-    }
-  }
-
-  __syncwarp();
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-}
-
-// ---------------------------------------------------------------- main, d = 128, overlapped
+// ---------------------------------------------------------------- main, overlapped
 //
-// Steps of 128 queries, so every product is an M = 128, N = 128 tcgen05.mma
+// Steps of 128 queries, so S^T and dP^T are M = 128, N = 128 tcgen05.mma
 // (a measured 8192 FLOP/clk/SM; N = 64 reaches only two thirds of that).
 // Two warpgroups recompute P and dS: group g owns the step's queries
-// [64g, 64g+64) and hands them to the tensor pipe in two quarters of 32, so
-// dV and dK of one quarter run while the next quarter is being recomputed.
-// dQ is produced transposed, dQ^T = K^T dS^T (M = d), into the dP^T columns
-// once both groups have read them, and drained while S^T of the next step runs.
-//   TMEM: S^T/P^T [0,128), dP^T/dQ^T [128,256), dV [256,384), dK [384,512).
+// [64g, 64g+64) and hands them to the tensor pipe in two quarters of 32, P
+// first (for dV) and dS after (for dK), so the products of one quarter run
+// while the next is being recomputed.
+// d = 128: dQ is produced transposed, dQ^T = K^T dS^T (M = d), into the dP^T
+// columns once both groups have read them, and drained while S^T of the next
+// step runs.  d = 64: dQ = dS K (M = 128 queries, N = 64) has columns of its own.
+//   TMEM: S^T/P^T [0,128), dP^T (d = 128: and dQ^T) [128,256), dV [256,256+d),
+//   dK [256+d,256+2d), dQ (d = 64) [384,448).
 //   P^T of query q sits at column 64*(q/64) + (q%64)/2: over the recomputing
 //   group's own, already-read S^T columns.
-//   Shared: K_j, V_j 32 KB each; two stages of Q_i, dO_i (32 KB each);
-//           dS^T 128 keys x 128 queries (two 64-query chunks).
-// Warps: 0-3 and 12-15 drain dQ^T (query columns 0-63 and 64-127), 4-11
-// recompute P and dS, 16 issues TMA loads, 17 owns TMEM and issues the MMAs.
+//   Shared: K_j, V_j (128 x d each); stages of Q_i, dO_i (two for d = 128,
+//           three for d = 64); dS^T 128 keys x 128 queries (two 64-query chunks).
+// Warps: 0-3 and 12-15 drain dQ (d = 128: query columns 0-63 and 64-127 of
+// dQ^T; d = 64: d columns 0-31 and 32-63 of dQ), 4-11 recompute P and dS,
+// 16 issues TMA loads, 17 owns TMEM and issues the MMAs.
 constexpr int kBwd128Threads = 576;
 constexpr int kWarpProducer = 16;
 constexpr int kWarpMma = 17;
 
+template <int D>
 struct Bwd128Layout {
-  static constexpr uint32_t kTile = 128u * 128u * 2u;  // 128 rows x 128 d
+  static constexpr uint32_t kTile = 128u * D * 2u;     // 128 rows x d
   static constexpr uint32_t kChunk = 128u * 128u;      // 128 rows x 64 columns
-  static constexpr int kStages = 2;
+  static constexpr int kStages = D == 64 ? 3 : 2;
   static constexpr uint32_t kK = 0;
   static constexpr uint32_t kV = kTile;
   static constexpr uint32_t kStage0 = 2 * kTile;
@@ -571,13 +227,13 @@ struct Bwd128Layout {
   static constexpr uint32_t kBytes = kBar + 256 + 1024 + 1024;  // barriers, lse2/D rows, alignment slack
 };
 
-template <int MASK>
+template <int D, int MASK>
 __global__ void __launch_bounds__(kBwd128Threads, 1)
-    fa_bwd_main128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    fa_bwd_main_ov_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                           const BwdParams p) {
-  using L = Bwd128Layout;
-  constexpr int D = 128;
+  using L = Bwd128Layout<D>;
+  constexpr int CH = D / 64;  // 128-byte swizzle columns per row
   constexpr int NST = L::kStages;
   constexpr uint32_t CHUNK = L::kChunk;
 
@@ -665,7 +321,7 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
       mbar_arrive_expect_tx(BAR(KV_FULL), 2 * L::kTile);
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < CH; ++c) {
         tma_load_4d(sK + c * CHUNK, &tm_k, BAR(KV_FULL), c * 64, kv_start + k0, h_kv, b_coord);
         tma_load_4d(sV + c * CHUNK, &tm_v, BAR(KV_FULL), c * 64, kv_start + k0, h_kv, b_coord);
       }
@@ -677,7 +333,7 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
         if (n >= NST && !(ok = mbar_wait(BAR(STAGE_EMPTY + st), ((n / NST) - 1) & 1, w, 51))) break;
         mbar_arrive_expect_tx(BAR(Q_FULL + st), 2 * L::kTile);
         const uint32_t qa = stage_q(st);
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < CH; ++c) {
           tma_load_4d(qa + c * CHUNK, &tm_q, BAR(Q_FULL + st), c * 64, row, hq, b_coord);
           tma_load_4d(qa + L::kTile + c * CHUNK, &tm_do, BAR(Q_FULL + st), c * 64, row, hq, b_coord);
         }
@@ -692,9 +348,10 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
     // ============================================================ MMA issuer
     if (lane == 0) {
       constexpr uint32_t IDESC_SD = idesc_bf16(128, 128, false, false);  // S^T, dP^T: M keys, N queries
-      constexpr uint32_t IDESC_KV = idesc_bf16(128, 128, false, true);   // dV, dK: M keys, N d
-      constexpr uint32_t IDESC_DQ = idesc_bf16(128, 128, true, true);    // dQ^T: M d, N queries
-      const uint32_t tS = tmem, tDP = tmem + 128, tDV = tmem + 256, tDK = tmem + 384;
+      constexpr uint32_t IDESC_KV = idesc_bf16(128, D, false, true);     // dV, dK: M keys, N d
+      // d = 128: dQ^T, M d, N queries, both operands MN-major; d = 64: dQ, M queries, N d, both MN-major
+      constexpr uint32_t IDESC_DQ = idesc_bf16(128, 128, true, true);
+      const uint32_t tS = tmem, tDP = tmem + 128, tDV = tmem + 256, tDK = tmem + 256 + D, tDQ = tmem + 384;
       // base descriptors; each product only advances the start address
       const uint64_t dK_kmaj = smem_desc_sw128(sK, 16, 1024);
       const uint64_t dV_kmaj = smem_desc_sw128(sV, 16, 1024);
@@ -712,18 +369,18 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
         const uint64_t q_mn = smem_desc_sw128(qa, CHUNK, 1024), do_mn = smem_desc_sw128(da, CHUNK, 1024);
         // S^T = K_j Q_i^T (the previous step's P^T was consumed by its dV products, issued earlier)
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * CHUNK + (kk % 4) * 32;
           mma_ss(tS, desc_add(dK_kmaj, off), desc_add(q_k, off), IDESC_SD, kk > 0);
         }
         mma_commit(BAR(S_FULL));  // P can be recomputed while dP^T is still running
-        if (n > 0) {  // the previous dQ^T must have left the dP^T columns
+        if (D == 128 && n > 0) {  // the previous dQ^T must have left the dP^T columns
           if (!(ok = mbar_wait(BAR(DQ_EMPTY), (n - 1) & 1, w, 54))) break;
           tc_fence_after();
         }
         // dP^T = V_j dO_i^T
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * CHUNK + (kk % 4) * 32;
           mma_ss(tDP, desc_add(dV_kmaj, off), desc_add(do_k, off), IDESC_SD, kk > 0);
         }
@@ -761,10 +418,23 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
         }
         if (!ok) break;
         mma_commit(BAR(STAGE_EMPTY + st));
-        // dQ^T = K_j^T dS^T (M = d, N = 128 queries over both dS^T chunks, K = 128 keys) into the dP^T columns
+        if constexpr (D == 128) {
+          // dQ^T = K_j^T dS^T (M = d, N = 128 queries over both dS^T chunks, K = 128 keys) into the dP^T columns
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tDP, desc_add(dK_mn, kk * 2048), desc_add(dDS_mn, kk * 2048), IDESC_DQ, kk > 0);
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tDP, desc_add(dK_mn, kk * 2048), desc_add(dDS_mn, kk * 2048), IDESC_DQ, kk > 0);
+        } else {
+          // dQ = dS K_j (M = 128 queries, N = d, K = 128 keys): A is dS^T read MN-major over the
+          // queries, B is K_j read MN-major over d; its own columns, free once the previous one is drained
+          if (n > 0) {
+            if (!(ok = mbar_wait(BAR(DQ_EMPTY), (n - 1) & 1, w, 54))) break;
+            tc_fence_after();
+          }
+          constexpr uint32_t IDESC_DQ64 = idesc_bf16(128, D, true, true);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tDQ, desc_add(dDS_mn, kk * 2048), desc_add(dK_mn, kk * 2048), IDESC_DQ64, kk > 0);
+        }
         mma_commit(BAR(DQ_FULL));
       }
       if (ok) mma_commit(BAR(DKV_FINAL));
@@ -898,7 +568,7 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
       if (__all_sync(0xffffffffu, ok)) {
         tc_fence_after();
         const size_t grow = ((size_t)b_coord * p.n_rows_k + kv_start + kg) * Hkv + h_kv;
-        const uint32_t src = tmem + lane_off + (g ? 384u : 256u);
+        const uint32_t src = tmem + lane_off + 256u + (g ? (uint32_t)D : 0u);
         __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(g ? p.dk : p.dv) + grow * D;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -914,6 +584,34 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
             for (int i = 0; i < 4; ++i) o4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
           }
         }
+      }
+    }
+  } else if (D == 64) {
+    // ============================================================ dQ drain, d = 64 (thread = one query row of dQ)
+    // warps 0-3 take d columns 0-31, warps 12-15 columns 32-63; float4 atomics into the
+    // [B*H][d/4][rows][4] accumulator (a warp's lanes, 32 consecutive rows, cover 512 bytes)
+    const int half = warp >= 12 ? 1 : 0;
+    const int qw = warp & 3;
+    const int qr = qw * 32 + lane;
+    const uint32_t src = tmem + ((uint32_t)(qw * 32) << 16) + 384 + 32 * half;
+    for (int n = 0; n < n_steps; ++n) {
+      float4* acc = reinterpret_cast<float4*>(p.dq_acc) + (size_t)(b_coord * p.H + hq_of(n)) * (D / 4) * p.n_rows;
+      const int qg = q_begin + (n % n_q) * 128 + qr;
+      bool ok = mbar_wait(BAR(DQ_FULL), n & 1, w, 60);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      uint32_t v[32];
+      tmem_ld32(src, v);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(BAR(DQ_EMPTY));  // the columns are free for the next dQ
+      if (qg < it.q_hi) {  // rows past q_hi see none of this block's keys: their share is zero
+        const size_t row = (size_t)seq_start + qg;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          atomicAdd(acc + (size_t)(8 * half + j) * p.n_rows + row,
+                    make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])));
       }
     }
   } else {
@@ -952,13 +650,9 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
   }
 }
 
-// d = 128 runs the overlapped kernel, d = 64 the serial one (only the chosen one is instantiated).
 template <int D, int MASK>
 static auto main_kernel_for() {
-  if constexpr (D == 128)
-    return fa_bwd_main128_kernel<MASK>;
-  else
-    return fa_bwd_main_kernel<D, MASK>;
+  return fa_bwd_main_ov_kernel<D, MASK>;
 }
 
 template <int D, int MASK>
@@ -972,7 +666,7 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
   if (e != cudaSuccess) return e;
 
   auto kern = main_kernel_for<D, MASK>();
-  constexpr uint32_t smem = D == 128 ? Bwd128Layout::kBytes : BwdLayout<D>::kBytes;
+  constexpr uint32_t smem = Bwd128Layout<D>::kBytes;
   static bool configured = false;
   if (!configured) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -982,7 +676,7 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
   const int bh = p.B * (p.H / p.kv_group);  // CTAs walk (batch, K/V head) pairs
   const int gx = bh < kBwdHeadGroup ? bh : kBwdHeadGroup;
   dim3 grid(gx, p.num_kblocks, (bh + gx - 1) / gx);
-  kern<<<grid, D == 128 ? kBwd128Threads : kBwdThreads, smem, stream>>>(tq, tk, tv, tdo, p);
+  kern<<<grid, kBwd128Threads, smem, stream>>>(tq, tk, tv, tdo, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
