@@ -300,6 +300,22 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float e0, float e1, float e2, fl
   return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
+// Cubic for 2^f on [0, 1) with c0 = 1 (minimax relative error 8.6e-5),
+// produced by fit_exp2_poly.py.
+constexpr float kExp2C1 = 6.951168240e-01f;
+constexpr float kExp2C2 = 2.276448658e-01f;
+constexpr float kExp2C3 = 7.706713327e-02f;
+
+// 2^x on the FMA pipe: the integer part goes straight into the exponent field.
+__device__ __forceinline__ float ex2_poly(float x) {
+  x = fmaxf(x, -127.0f);
+  const float t = __fadd_rd(x, 12582912.0f);  // 1.5 * 2^23: floor(x) lands in the low mantissa bits
+  const float fl = t - 12582912.0f;           // floor(x), exact
+  const float f = x - fl;                      // [0, 1)
+  const float p = fmaf(fmaf(fmaf(kExp2C3, f, kExp2C2), f, kExp2C1), f, 1.0f);
+  return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
