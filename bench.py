@@ -166,7 +166,7 @@ def run_ours(args):
     import torch.distributed as dist
 
     import synth
-    from exact_attention_94_gb300 import _lib, accounting as acc, ops
+    from exact_attention_94_gb300 import _lib, accounting as acc, ops, replicas
 
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
@@ -224,16 +224,13 @@ def run_ours(args):
     fwd_ms = [inner.ev[i * per].elapsed_time(inner.ev[i * per + 1]) for i in range(args.steps)]
     bwd_ms = ([inner.ev[i * per + 1].elapsed_time(inner.ev[i * per + 2]) for i in range(args.steps)]
               if have_bwd else [0.0])
-    if world > 1:
-        t = torch.tensor([total_ms, statistics.mean(fwd_ms), statistics.mean(bwd_ms)], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, fwd_mean, bwd_mean = t.tolist()
-    else:
-        fwd_mean, bwd_mean = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
+    # the slowest rank sets every time (a no-op on one process)
+    total_ms, fwd_mean, bwd_mean = replicas.max_over_ranks(
+        [total_ms, statistics.mean(fwd_ms), statistics.mean(bwd_ms)], device="cuda")
     assert ops.device_error() == 0, "a bounded wait ran out inside a kernel"
     ms_step = total_ms / args.steps
     step_flops = F * (2.5 if have_bwd else 1.0)     # literal reading: fwd+bwd = 2.5x the forward
-    value = world * step_flops / (ms_step * 1e-3) / 1e12
+    value = replicas.whole_job_rate(world, step_flops, ms_step) / 1e12
     fwd_tf = F / (fwd_mean * 1e-3) / 1e12
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -544,13 +541,14 @@ def main():
     import torch
     import torch.distributed as dist
 
+    from exact_attention_94_gb300 import replicas
+
     res, ctx = run_ours(args)
     e2e = run_e2e(args, ctx)
     if world > 1:
-        t = torch.tensor([e2e["ms_per_step"]], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e["value"] = round(world * float(e2e["value"]) * e2e["ms_per_step"] / float(t.item()), 2)
-        e2e["ms_per_step"] = round(float(t.item()), 4)
+        (slowest,) = replicas.max_over_ranks([e2e["ms_per_step"]], device="cuda")
+        e2e["value"] = round(replicas.rescale_to_slowest(float(e2e["value"]), e2e["ms_per_step"], slowest, world), 2)
+        e2e["ms_per_step"] = round(slowest, 4)
     res["e2e"] = e2e
     del ctx
     torch.cuda.empty_cache()
