@@ -47,6 +47,8 @@ SIGNATURES = {
     "fa_pool_export": (_I, [_P, _P, _P]),
     "fa_paged_append": (_I, [_P] * 7 + [_I] * 5 + [_P]),
     "fa_decode_workspace_bytes": (_S, [_I, _I, _I, _I]),
+    "fa_decode_window": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _F, _P]),
+    "fa_decode_paged_window": (_I, [_P] * 7 + [_I] * 10 + [_P, _F, _P]),
     "fa_decode_num_splits": (_I, [_I, _I, _I, _I]),
     "fa_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _F, _P]),
     "fa_decode_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _F, _P]),

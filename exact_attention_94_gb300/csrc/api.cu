@@ -562,9 +562,11 @@ int fa_decode_num_splits(int B, int H, int L, int d) {
 static fa_status decode_common(const void* q, const void* k, const void* v, const int* block_table,
                                const int* seq_lens, int page_size, int num_pages, int max_blocks, void* o, float* lse,
                                int B, int H, int Hkv, int L, int d, int num_splits, void* workspace, float scale,
-                               fa_stream_t stream) {
+                               fa_stream_t stream, int win_left = -1) {
   if (!q || !o || !lse || !workspace) return FA_ERR_INVALID_ARG;
-  if (B < 1 || H < 1 || Hkv < 1 || H % Hkv != 0 || L < 0 || num_splits < 0) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || Hkv < 1 || H % Hkv != 0 || L < 0 || num_splits < 0 || win_left < -1) return FA_ERR_INVALID_ARG;
+  if (win_left >= L) win_left = -1;  // a window past every key is no window
+  const int span = win_left >= 0 ? win_left + 1 : L;  // keys a query sees at most
   const int group = H / Hkv;
   if (group > 32) return FA_ERR_UNSUPPORTED;  // a CTA serves at most 32 query heads
   if (L > 0 && (!k || !v)) return FA_ERR_INVALID_ARG;  // an empty contiguous cache may be null
@@ -573,8 +575,8 @@ static fa_status decode_common(const void* q, const void* k, const void* v, cons
   const void* ptrs[] = {q, k, v, o, lse, workspace};
   for (const void* ptr : ptrs)
     if (!aligned16(ptr)) return FA_ERR_MISALIGNED;
-  const int S = num_splits > 0 ? num_splits : auto_splits(B, Hkv, group, L);
-  if (L > 0 && S > L) return FA_ERR_INVALID_ARG;
+  const int S = num_splits > 0 ? num_splits : auto_splits(B, Hkv, group, span);
+  if (L > 0 && S > span) return FA_ERR_INVALID_ARG;
   const int G = decode_group(Hkv, group);
   if (B > 65535 || Hkv / G > 65535) return FA_ERR_INVALID_ARG;
   if (!ensure_init()) return FA_ERR_LAUNCH;
@@ -592,7 +594,8 @@ static fa_status decode_common(const void* q, const void* k, const void* v, cons
   p.kv_group = group;
   p.L = L;
   p.G = G;
-  p.chunk = L > 0 ? (L + S - 1) / S : 0;
+  p.chunk = span > 0 ? (span + S - 1) / S : 0;
+  p.win_left = win_left;
   p.num_splits = S;
   p.stages = decode_stages(G, d);
   p.block_table = block_table;
@@ -619,6 +622,27 @@ fa_status fa_decode_paged(const void* q, const void* k_pages, const void* v_page
     return FA_ERR_MISALIGNED;
   return decode_common(q, k_pages, v_pages, block_table, seq_lens, page_size, num_pages, max_blocks, o, lse, B, H, H,
                        max_seq_len, d, num_splits, workspace, scale, stream);
+}
+
+fa_status fa_decode_window(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse, int B, int Hq,
+                           int Hkv, int L, int d, int window_left, int num_splits, void* workspace, float scale,
+                           fa_stream_t stream) {
+  return decode_common(q, k_cache, v_cache, nullptr, nullptr, 0, 0, 0, o, lse, B, Hq, Hkv, L, d, num_splits,
+                       workspace, scale, stream, window_left);
+}
+
+fa_status fa_decode_paged_window(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
+                                 const int* seq_lens, void* o, float* lse, int B, int Hq, int Hkv, int d,
+                                 int page_size, int num_pages, int max_blocks, int max_seq_len, int window_left,
+                                 int num_splits, void* workspace, float scale, fa_stream_t stream) {
+  if (!k_pages || !v_pages || !block_table || !seq_lens) return FA_ERR_INVALID_ARG;
+  if (num_pages < 1 || max_blocks < 1 || max_seq_len < 0) return FA_ERR_INVALID_ARG;
+  if (page_size < 4 || page_size % 4 != 0 || (long long)max_blocks * page_size < max_seq_len)
+    return FA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return FA_ERR_MISALIGNED;
+  return decode_common(q, k_pages, v_pages, block_table, seq_lens, page_size, num_pages, max_blocks, o, lse, B, Hq,
+                       Hkv, max_seq_len, d, num_splits, workspace, scale, stream, window_left);
 }
 
 fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse, int B,

@@ -84,7 +84,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) fa_decode_split_kernel(const D
       L_b = L_b < 0 ? 0 : p.L;
     }
   }
-  const int l0 = c * p.chunk;
+  // a sliding window keeps the last win_left + 1 keys: the splits cover [kbeg, L_b)
+  const int kbeg = p.win_left >= 0 ? max(0, L_b - 1 - p.win_left) : 0;
+  const int l0 = kbeg + c * p.chunk;
   const int l1 = min(L_b, l0 + p.chunk);
   const int n_keys = max(0, l1 - l0);
   const int n_st = (n_keys + kDecT - 1) / kDecT;

@@ -135,6 +135,7 @@ struct DecodeParams {
   int page_size;
   int max_blocks;
   int num_pages;
+  int win_left;              // sliding window: only keys >= len - 1 - win_left are seen (-1: all)
   float scale_log2;
   unsigned* err;
   unsigned long long timeout_ns;

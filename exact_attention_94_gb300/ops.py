@@ -506,3 +506,66 @@ def paged_append(k_new, v_new, k_pages, v_pages, page, slot, copy_src, stream=No
     st = lib().fa_paged_append(_ptr(k_new), _ptr(v_new), _ptr(k_pages), _ptr(v_pages), _ptr(page), _ptr(slot),
                                _ptr(copy_src), n, Hkv, d, P, num_pages, _stream(stream))
     _lib.check(st, "fa_paged_append")
+
+
+# ---------------------------------------------------------------- decode with a sliding window
+
+def _window_span(L: int, window_left: int) -> int:
+    return L if window_left < 0 or window_left >= L else window_left + 1
+
+
+def decode_window(q, k_cache, v_cache, window_left: int, num_splits: int = 0, scale: Optional[float] = None,
+                  stream=None):
+    """Decode that sees only the last window_left + 1 keys of each cache.
+    q [B, 1, Hq, d]; caches [B, L, Hkv, d].  Returns (o [B, 1, Hq, d], lse [B, Hq])."""
+    _check_bf16("q", q)
+    B, one, Hq, d = q.shape
+    _check_bf16("k_cache", k_cache)
+    L, Hkv = k_cache.shape[1], k_cache.shape[2]
+    if one != 1 or tuple(k_cache.shape) != (B, L, Hkv, d):
+        raise ValueError("q must be [B, 1, Hq, d] and the caches [B, L, Hkv, d]")
+    _check_bf16("v_cache", v_cache, k_cache.shape)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    span = _window_span(L, int(window_left))
+    splits = num_splits if num_splits > 0 else lib().fa_decode_num_splits(B, Hkv, span, d)
+    nbytes = lib().fa_decode_workspace_bytes(B, Hq, d, max(splits, 1))
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    o = torch.empty_like(q)
+    l = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    st = lib().fa_decode_window(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(l), B, Hq, Hkv, L, d,
+                                int(window_left), splits, _ptr(ws), scale, _stream(stream))
+    _lib.check(st, "fa_decode_window")
+    return o, l
+
+
+def decode_paged_window(q, k_pages, v_pages, block_table, seq_lens, max_seq_len: int, window_left: int = -1,
+                        num_splits: int = 0, scale: Optional[float] = None, stream=None):
+    """Paged decode with grouped K/V heads and a sliding window.  q [B, 1, Hq, d];
+    pages [num_pages, page_size, Hkv, d]; block_table int32 [B, max_blocks] and
+    seq_lens int32 [B] on the device.  Returns (o [B, 1, Hq, d], lse [B, Hq])."""
+    _check_bf16("q", q)
+    B, one, Hq, d = q.shape
+    if one != 1:
+        raise ValueError("q must be [B, 1, Hq, d]")
+    _check_bf16("k_pages", k_pages)
+    num_pages, page_size, Hkv = k_pages.shape[0], k_pages.shape[1], k_pages.shape[2]
+    if tuple(k_pages.shape) != (num_pages, page_size, Hkv, d):
+        raise ValueError("k_pages must be [num_pages, page_size, Hkv, d]")
+    _check_bf16("v_pages", v_pages, k_pages.shape)
+    for name, t in (("block_table", block_table), ("seq_lens", seq_lens)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
+    if block_table.dim() != 2 or block_table.shape[0] != B or tuple(seq_lens.shape) != (B,):
+        raise ValueError("block_table must be [B, max_blocks] and seq_lens [B]")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    span = _window_span(int(max_seq_len), int(window_left))
+    splits = num_splits if num_splits > 0 else lib().fa_decode_num_splits(B, Hkv, span, d)
+    nbytes = lib().fa_decode_workspace_bytes(B, Hq, d, max(splits, 1))
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    o = torch.empty_like(q)
+    l = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    st = lib().fa_decode_paged_window(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seq_lens),
+                                      _ptr(o), _ptr(l), B, Hq, Hkv, d, page_size, num_pages, block_table.shape[1],
+                                      int(max_seq_len), int(window_left), splits, _ptr(ws), scale, _stream(stream))
+    _lib.check(st, "fa_decode_paged_window")
+    return o, l

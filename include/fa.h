@@ -394,6 +394,32 @@ fa_status fa_decode_paged(const void* q, const void* k_pages, const void* v_page
                           fa_stream_t stream);
 
 /*
+ * Decode with a sliding window ("efficient-attention/flash-2-3", section
+ * "Using it, the real way": FlashAttention kernels support sliding windows):
+ * the single query of sequence b sits at key position len - 1 and sees keys
+ * len - 1 - window_left .. len - 1 (window_left = -1: all of them, as
+ * fa_decode_gqa).  The splits cover the window only, so a long cache costs
+ * what its window does.
+ *   window_left : >= -1; a window past every key is no window
+ *   workspace   : fa_decode_workspace_bytes(B, Hq, d, splits)
+ * Otherwise as fa_decode_gqa.
+ */
+fa_status fa_decode_window(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse, int B, int Hq,
+                           int Hkv, int L, int d, int window_left, int num_splits, void* workspace, float scale,
+                           fa_stream_t stream);
+
+/*
+ * fa_decode_paged with grouped K/V heads and a sliding window: q [B, 1, Hq, d],
+ * k_pages, v_pages [num_pages, page_size, Hkv, d] (Hkv divides Hq, Hq / Hkv <= 32);
+ * sequence b sees its keys seq_lens[b] - 1 - window_left .. seq_lens[b] - 1
+ * (window_left = -1: all).  Otherwise as fa_decode_paged.
+ */
+fa_status fa_decode_paged_window(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
+                                 const int* seq_lens, void* o, float* lse, int B, int Hq, int Hkv, int d,
+                                 int page_size, int num_pages, int max_blocks, int max_seq_len, int window_left,
+                                 int num_splits, void* workspace, float scale, fa_stream_t stream);
+
+/*
  * Synchronises the device, then returns FA_OK if no kernel of this library
  * recorded an error since the last call, FA_ERR_TIMEOUT if a bounded wait ran
  * out (code 0x1000 + wait site), FA_ERR_INVALID_ARG if a kernel met a bad

@@ -141,3 +141,48 @@ def test_paged_bad_table_entry_is_reported_not_read():
     torch.cuda.synchronize()
     assert ops.device_error() == 0x2000
     assert ops.device_error() == 0
+
+
+# ---------------------------------------------------------------- sliding window, grouped heads
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("wl", [0, 5, 127, 300, 5000, -1])
+@pytest.mark.parametrize("num_splits", [0, 1, 3])
+def test_decode_window(d, wl, num_splits):
+    """Keys len-1-wl .. len-1 only; against the masked oracle with one query."""
+    B, Hq, Hkv, L = 3, 8, 2, 1000
+    g = torch.Generator().manual_seed(wl + 7 + d)
+    q = torch.randn((B, 1, Hq, d), generator=g).to(torch.bfloat16)
+    kc = torch.randn((B, L, Hkv, d), generator=g).to(torch.bfloat16)
+    vc = torch.randn((B, L, Hkv, d), generator=g).to(torch.bfloat16)
+    span = L if wl < 0 or wl >= L else wl + 1
+    if num_splits > span:
+        pytest.skip("more splits than keys in the window")
+    o, lse = ops.decode_window(q.cuda(), kc.cuda(), vc.cuda(), wl, num_splits=num_splits)
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    o_ref, l_ref = oracle.masked_forward(synth.to_f64(q), synth.to_f64(kc), synth.to_f64(vc), 1 / math.sqrt(d), wl, 0)
+    assert_o(synth.to_f64(o), o_ref, f"window decode wl{wl}")
+    assert_lse(lse.cpu().numpy(), l_ref[:, :, 0], f"window decode wl{wl}")
+
+
+@pytest.mark.parametrize("wl", [-1, 40, 17])
+def test_paged_decode_window_grouped(wl):
+    """Ragged paged caches, 4 query heads per K/V head, a window."""
+    lengths = [1, 15, 16, 17, 100, 1000]
+    Hq, Hkv, d, P = 8, 2, 128, 16
+    x = synth.make_paged_decode(lengths, Hkv, d, page_size=P, seed=wl + 50)
+    g = torch.Generator().manual_seed(wl + 51)
+    q = torch.randn((len(lengths), 1, Hq, d), generator=g).to(torch.bfloat16)
+    dev = {n: x[n].cuda() for n in x}
+    o, lse = ops.decode_paged_window(q.cuda(), dev["k_pages"], dev["v_pages"], dev["block_table"], dev["seq_lens"],
+                                     max(lengths), wl, num_splits=3)
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    kp, vp = synth.to_f64(x["k_pages"]), synth.to_f64(x["v_pages"])
+    for b, Lb in enumerate(lengths):
+        kb = oracle.gather_pages(kp, x["block_table"][b].numpy(), Lb)[None]
+        vb = oracle.gather_pages(vp, x["block_table"][b].numpy(), Lb)[None]
+        o_ref, l_ref = oracle.masked_forward(synth.to_f64(q[b:b + 1]), kb, vb, 1 / math.sqrt(d), wl, 0)
+        assert_o(synth.to_f64(o[b:b + 1]), o_ref, f"paged window b{b}")
+        assert_lse(lse[b:b + 1].cpu().numpy(), l_ref[:, :, 0], f"paged window b{b}")
