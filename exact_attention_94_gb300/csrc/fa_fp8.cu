@@ -5,7 +5,7 @@
 // matrix times a random +-1 diagonal before quantising).
 //
 // One CTA per 128-row block of one (batch, head); warp w owns rows
-// 16w .. 16w+15, a row is spread over d/16 lanes of 16 consecutive columns.
+// 8w .. 8w+7, a row is spread over d/16 lanes of 16 consecutive columns.
 //   rotate:   x <- (x H) * signs, H the Sylvester-Hadamard matrix (entries
 //             +-1), by the fast transform: stage widths 1, 2, 4, ..., d/2, each
 //             butterfly (a, b) -> (a + b, a - b) in fp32.  Widths below 16
@@ -25,7 +25,8 @@ namespace fa {
 
 namespace {
 
-constexpr int kQuantThreads = 256;  // 8 warps; each takes 16 rows of the 128-row block
+constexpr int kQuantThreads = 512;  // 16 warps; each takes 8 rows of the 128-row block
+constexpr int kRowsPerWarp = kQuantThreads == 512 ? 8 : 16;
 constexpr int kElems = 16;          // consecutive elements per lane
 
 // Butterflies of widths 1 .. 8 inside the lane's 16 elements, then widths
@@ -64,7 +65,7 @@ __global__ void __launch_bounds__(kQuantThreads) fa_fp8_quant_kernel(const __nv_
                                                                      int nblk) {
   constexpr int LPR = D / kElems;   // lanes per row
   constexpr int RPI = 32 / LPR;     // rows per warp and iteration
-  constexpr int IT = 16 / RPI;      // iterations: 16 rows per warp
+  constexpr int IT = kRowsPerWarp / RPI;  // iterations over the warp's rows
   const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int seg = lane % LPR;       // which 16 columns of the row
@@ -82,7 +83,7 @@ __global__ void __launch_bounds__(kQuantThreads) fa_fp8_quant_kernel(const __nv_
   float amax = 0.f;
 #pragma unroll
   for (int it = 0; it < IT; ++it) {
-    const int n = blk * 128 + warp * 16 + it * RPI + sub;
+    const int n = blk * 128 + warp * kRowsPerWarp + it * RPI + sub;
     if (n < N) {
       const uint4* src = reinterpret_cast<const uint4*>(x + (((size_t)b * N + n) * H + h) * D + seg * kElems);
       const uint4 w0 = src[0], w1 = src[1];
@@ -119,7 +120,7 @@ __global__ void __launch_bounds__(kQuantThreads) fa_fp8_quant_kernel(const __nv_
 
 #pragma unroll
   for (int it = 0; it < IT; ++it) {
-    const int rr = warp * 16 + it * RPI + sub;  // row within the block
+    const int rr = warp * kRowsPerWarp + it * RPI + sub;  // row within the block
     const int n = blk * 128 + rr;
     uint32_t wd[4];
 #pragma unroll
