@@ -44,8 +44,11 @@ struct Options {
 
 std::once_flag g_init_once;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-unsigned* g_err_ptr = nullptr;
-bool g_init_ok = false;
+
+constexpr int kMaxErrDevices = 64;
+std::mutex g_err_mutex;
+unsigned* g_err_ptrs[kMaxErrDevices] = {};   // device address of g_fa_error, per device ordinal
+thread_local unsigned* g_err_ptr = nullptr;  // the current device's, set by ensure_init()
 
 void init_once() {
   cudaDriverEntryPointQueryResult q;
@@ -54,14 +57,24 @@ void init_once() {
           cudaSuccess &&
       q == cudaDriverEntryPointSuccess)
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  void* ep = nullptr;
-  if (cudaGetSymbolAddress(&ep, g_fa_error) == cudaSuccess) g_err_ptr = static_cast<unsigned*>(ep);
-  g_init_ok = g_encode != nullptr && g_err_ptr != nullptr;
 }
 
+// Every entry point calls this before it builds kernel parameters: it resolves
+// the driver entry point once per process and the error word's device address
+// once per device (the symbol has an address of its own on each device).
 bool ensure_init() {
   std::call_once(g_init_once, init_once);
-  return g_init_ok;
+  if (g_encode == nullptr) return false;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxErrDevices) return false;
+  std::lock_guard<std::mutex> lock(g_err_mutex);
+  if (g_err_ptrs[dev] == nullptr) {
+    void* ep = nullptr;
+    if (cudaGetSymbolAddress(&ep, g_fa_error) != cudaSuccess || ep == nullptr) return false;
+    g_err_ptrs[dev] = static_cast<unsigned*>(ep);
+  }
+  g_err_ptr = g_err_ptrs[dev];
+  return true;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

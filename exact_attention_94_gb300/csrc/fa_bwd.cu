@@ -667,11 +667,13 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
 
   auto kern = main_kernel_for<D, MASK>();
   constexpr uint32_t smem = Bwd128Layout<D>::kBytes;
-  static bool configured = false;
-  if (!configured) {
+  static bool configured[64] = {};  // the shared-memory limit is a per-device function attribute
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured[dev] = true;
   }
   const int bh = p.B * (p.H / p.kv_group);  // CTAs walk (batch, K/V head) pairs
   const int gx = bh < kBwdHeadGroup ? bh : kBwdHeadGroup;

@@ -496,11 +496,13 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
                                 const FwdParams& p, int grid_x, cudaStream_t stream) {
   auto kern = fa_fwd_kernel<D, MASK, POLY, F8>;
   constexpr uint32_t smem = FwdLayout<D, F8>::kBytes;
-  static bool configured = false;
-  if (!configured) {
+  static bool configured[64] = {};  // the shared-memory limit is a per-device function attribute
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured[dev] = true;
   }
   const int gx = grid_x < kHeadGroup ? grid_x : kHeadGroup;
   dim3 grid(gx, p.num_pairs, (grid_x + gx - 1) / gx);
