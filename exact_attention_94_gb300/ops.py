@@ -8,6 +8,7 @@ arithmetic happens in the library's CUDA kernels.
 from __future__ import annotations
 
 import ctypes
+import functools
 import math
 from typing import Optional, Tuple
 
@@ -34,6 +35,22 @@ def _stream(stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+def _on_tensor_device(fn):
+    """Runs a wrapper with the CUDA device of its tensors current (the library
+    launches on the current device); tensors on two devices are refused."""
+    @functools.wraps(fn)
+    def wrapper(*args, **kwargs):
+        tensors = [a for a in list(args) + list(kwargs.values()) if isinstance(a, torch.Tensor) and a.is_cuda]
+        if not tensors:
+            return fn(*args, **kwargs)
+        dev = tensors[0].device
+        if any(t.device != dev for t in tensors):
+            raise ValueError("all CUDA tensors of a call must be on one device")
+        with torch.cuda.device(dev):
+            return fn(*args, **kwargs)
+    return wrapper
+
+
 def _check_bf16(name, t, shape=None):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
@@ -58,6 +75,7 @@ def device_error() -> int:
     return int(code.value)
 
 
+@_on_tensor_device
 def fwd(q, k, v, causal: bool = False, scale: Optional[float] = None, out=None, lse=None,
         stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Dense forward.  q, k, v [B, N, H, d] bf16 -> (o [B, N, H, d], lse [B, H, N] fp32)."""
@@ -75,6 +93,7 @@ def fwd(q, k, v, causal: bool = False, scale: Optional[float] = None, out=None, 
     return o, l
 
 
+@_on_tensor_device
 def bwd(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float] = None, workspace=None,
         stream=None, out=None):
     """Dense backward -> (dq, dk, dv), each [B, N, H, d] bf16 (written into
@@ -108,6 +127,7 @@ def _check_cu(cu_seqlens, q):
         raise ValueError("cu_seqlens must be on the device of q")
 
 
+@_on_tensor_device
 def fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False, scale: Optional[float] = None,
                stream=None):
     """Packed forward.  q, k, v [total, H, d]; cu_seqlens int32 [S+1] on the device.
@@ -126,6 +146,7 @@ def fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False, scale
     return o, l
 
 
+@_on_tensor_device
 def bwd_varlen(q, k, v, o, lse, dout, cu_seqlens, max_seqlen: int, causal: bool = False,
                scale: Optional[float] = None, stream=None):
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
@@ -145,6 +166,7 @@ def bwd_varlen(q, k, v, o, lse, dout, cu_seqlens, max_seqlen: int, causal: bool 
     return dq, dk, dv
 
 
+@_on_tensor_device
 def decode(q, k_cache, v_cache, num_splits: int = 0, scale: Optional[float] = None, stream=None,
            workspace=None):
     """Single-token decode.  q [B, 1, H, d]; caches [B, L, H, d].
@@ -170,6 +192,7 @@ def decode(q, k_cache, v_cache, num_splits: int = 0, scale: Optional[float] = No
     return o, l
 
 
+@_on_tensor_device
 def decode_paged(q, k_pages, v_pages, block_table, seq_lens, max_seq_len: int, num_splits: int = 0,
                  scale: Optional[float] = None, stream=None, workspace=None):
     """Single-token decode over a paged cache.  q [B, 1, H, d]; pages
@@ -204,6 +227,7 @@ def decode_paged(q, k_pages, v_pages, block_table, seq_lens, max_seq_len: int, n
 
 # ---------------------------------------------------------------- grouped-query attention
 
+@_on_tensor_device
 def fwd_gqa(q, k, v, causal: bool = False, scale: Optional[float] = None, stream=None):
     """q [B, N, Hq, d]; k, v [B, N, Hkv, d] with Hkv dividing Hq.
     Returns (o [B, N, Hq, d], lse [B, Hq, N])."""
@@ -223,6 +247,7 @@ def fwd_gqa(q, k, v, causal: bool = False, scale: Optional[float] = None, stream
     return o, l
 
 
+@_on_tensor_device
 def bwd_gqa(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float] = None, stream=None):
     """Gradients of fwd_gqa: (dq [B, N, Hq, d], dk, dv [B, N, Hkv, d])."""
     for name, t in (("q", q), ("o", o), ("dout", dout)):
@@ -241,6 +266,7 @@ def bwd_gqa(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float] 
     return dq, dk, dv
 
 
+@_on_tensor_device
 def decode_gqa(q, k_cache, v_cache, num_splits: int = 0, scale: Optional[float] = None, stream=None):
     """q [B, 1, Hq, d]; caches [B, L, Hkv, d].  Returns (o [B, 1, Hq, d], lse [B, Hq])."""
     _check_bf16("q", q)
@@ -274,6 +300,7 @@ def _window(causal: bool, window: Optional[Tuple[int, int]]):
     return wl, wr
 
 
+@_on_tensor_device
 def fwd_masked(q, k, v, causal: bool = False, window: Optional[Tuple[int, int]] = None,
                scale: Optional[float] = None, stream=None):
     """q [B, Nq, Hq, d]; k, v [B, Nk, Hkv, d].  Bottom-right aligned mask:
@@ -297,6 +324,7 @@ def fwd_masked(q, k, v, causal: bool = False, window: Optional[Tuple[int, int]] 
     return o, l
 
 
+@_on_tensor_device
 def bwd_masked(q, k, v, o, lse, dout, causal: bool = False, window: Optional[Tuple[int, int]] = None,
                scale: Optional[float] = None, stream=None):
     """Gradients of fwd_masked: (dq [B, Nq, Hq, d], dk, dv [B, Nk, Hkv, d])."""
@@ -319,6 +347,7 @@ def bwd_masked(q, k, v, o, lse, dout, causal: bool = False, window: Optional[Tup
     return dq, dk, dv
 
 
+@_on_tensor_device
 def fwd_masked_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
                       causal: bool = False, window: Optional[Tuple[int, int]] = None,
                       scale: Optional[float] = None, stream=None):
@@ -346,6 +375,7 @@ def fwd_masked_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, ma
     return o, l
 
 
+@_on_tensor_device
 def bwd_masked_varlen(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
                       causal: bool = False, window: Optional[Tuple[int, int]] = None,
                       scale: Optional[float] = None, stream=None):
@@ -375,6 +405,7 @@ def bwd_masked_varlen(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seq
 
 # ---------------------------------------------------------------- FP8 forward
 
+@_on_tensor_device
 def fp8_quantize(x, signs=None, transpose: bool = False, stream=None):
     """e4m3 block quantisation of x [B, N, H, d] (bf16).  With ``signs`` (int8
     [d] of +-1 on the device) the rows are first rotated by the Hadamard matrix
@@ -397,6 +428,7 @@ def fp8_quantize(x, signs=None, transpose: bool = False, stream=None):
     return codes, scales
 
 
+@_on_tensor_device
 def fwd_fp8_codes(q_codes, k_codes, vt_codes, q_scale, k_scale, v_scale, causal: bool = False,
                   window: Optional[Tuple[int, int]] = None, rotated: bool = True, scale: Optional[float] = None,
                   stream=None):
@@ -420,6 +452,7 @@ def fwd_fp8_codes(q_codes, k_codes, vt_codes, q_scale, k_scale, v_scale, causal:
     return o, l
 
 
+@_on_tensor_device
 def fwd_fp8(q, k, v, signs=None, causal: bool = False, window: Optional[Tuple[int, int]] = None,
             scale: Optional[float] = None, stream=None):
     """The FP8 forward from bf16 inputs: quantise Q and K (rotated when signs
@@ -489,6 +522,7 @@ class PagePool:
         return table, lens
 
 
+@_on_tensor_device
 def paged_append(k_new, v_new, k_pages, v_pages, page, slot, copy_src, stream=None):
     """Copies shared pages where copy_src >= 0, then writes each token's K, V
     rows ([n, Hkv, d] bf16) into (page, slot); index tensors int32 on the device."""
@@ -514,6 +548,7 @@ def _window_span(L: int, window_left: int) -> int:
     return L if window_left < 0 or window_left >= L else window_left + 1
 
 
+@_on_tensor_device
 def decode_window(q, k_cache, v_cache, window_left: int, num_splits: int = 0, scale: Optional[float] = None,
                   stream=None):
     """Decode that sees only the last window_left + 1 keys of each cache.
@@ -538,6 +573,7 @@ def decode_window(q, k_cache, v_cache, window_left: int, num_splits: int = 0, sc
     return o, l
 
 
+@_on_tensor_device
 def decode_paged_window(q, k_pages, v_pages, block_table, seq_lens, max_seq_len: int, window_left: int = -1,
                         num_splits: int = 0, scale: Optional[float] = None, stream=None):
     """Paged decode with grouped K/V heads and a sliding window.  q [B, 1, Hq, d];
