@@ -129,13 +129,13 @@ struct DecodeParams {
   int chunk;                 // keys per split
   int num_splits;
   int stages;                // shared-memory ring depth
+  int win_left;              // sliding window: only keys >= len - 1 - win_left are seen (-1: all)
   // paged cache (block_table == nullptr: contiguous [B, L, H, d] cache)
   const int* block_table;    // [B, max_blocks] physical page of each logical block of page_size keys
   const int* seq_lens;       // [B] keys of each sequence (<= L)
   int page_size;
   int max_blocks;
   int num_pages;
-  int win_left;              // sliding window: only keys >= len - 1 - win_left are seen (-1: all)
   float scale_log2;
   unsigned* err;
   unsigned long long timeout_ns;
