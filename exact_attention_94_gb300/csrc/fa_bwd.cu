@@ -271,7 +271,8 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
   auto hq_of = [&](int n) { return h_kv * p.kv_group + n / n_q; };
   auto row_base_of = [&](int hq) { return (size_t)(b_coord * p.H + hq) * p.n_rows + seq_start; };
 
-  enum { KV_FULL = 0, Q_FULL = 1, STAGE_EMPTY = Q_FULL + NST, S_FULL = STAGE_EMPTY + NST, DP_FULL = S_FULL + 1,
+  enum { KV_FULL = 0, Q_FULL = 1, DO_FULL = Q_FULL + NST, STAGE_EMPTY = DO_FULL + NST, S_FULL = STAGE_EMPTY + NST,
+         DP_FULL = S_FULL + 1,
          P_READY = DP_FULL + 1, DS_READY = P_READY + 4,
          DQ_FULL = DS_READY + 4, DQ_EMPTY, DKV_FINAL, DRAIN, NBARS };
   const uint32_t bar0 = base + L::kBar;
@@ -285,6 +286,7 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
     mbar_init(BAR(KV_FULL), 1);
     for (int s = 0; s < NST; ++s) {
       mbar_init(BAR(Q_FULL + s), 1);
+      mbar_init(BAR(DO_FULL + s), 1);
       mbar_init(BAR(STAGE_EMPTY + s), 1);
     }
     mbar_init(BAR(S_FULL), 1);
@@ -331,12 +333,13 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
         const int row = seq_start + q_begin + (n % n_q) * 128;
         const int hq = hq_of(n);
         if (n >= NST && !(ok = mbar_wait(BAR(STAGE_EMPTY + st), ((n / NST) - 1) & 1, w, 51))) break;
-        mbar_arrive_expect_tx(BAR(Q_FULL + st), 2 * L::kTile);
         const uint32_t qa = stage_q(st);
-        for (int c = 0; c < CH; ++c) {
-          tma_load_4d(qa + c * CHUNK, &tm_q, BAR(Q_FULL + st), c * 64, row, hq, b_coord);
-          tma_load_4d(qa + L::kTile + c * CHUNK, &tm_do, BAR(Q_FULL + st), c * 64, row, hq, b_coord);
-        }
+        // Q_i first: S^T of a step is issued while the previous step's products still run
+        mbar_arrive_expect_tx(BAR(Q_FULL + st), L::kTile);
+        for (int c = 0; c < CH; ++c) tma_load_4d(qa + c * CHUNK, &tm_q, BAR(Q_FULL + st), c * 64, row, hq, b_coord);
+        mbar_arrive_expect_tx(BAR(DO_FULL + st), L::kTile);
+        for (int c = 0; c < CH; ++c)
+          tma_load_4d(qa + L::kTile + c * CHUNK, &tm_do, BAR(DO_FULL + st), c * 64, row, hq, b_coord);
       }
       if (!ok) {
         const uint64_t t0 = globaltimer_ns();
@@ -360,35 +363,33 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
       const uint64_t dDS_mn = smem_desc_sw128(sDS, CHUNK, 1024); // dS^T as MN-major B over queries
       bool ok = mbar_wait(BAR(KV_FULL), 0, w, 52);
       tc_fence_after();
-      for (int n = 0; n < n_steps && ok; ++n) {
+      // S^T(n) = K_j Q_n^T into columns [0,128)
+      auto issue_s = [&](int n) {
         const int st = n % NST;
-        const uint32_t qa = stage_q(st), da = qa + L::kTile;
-        if (!(ok = mbar_wait(BAR(Q_FULL + st), (n / NST) & 1, w, 53))) break;
+        if (!(ok = mbar_wait(BAR(Q_FULL + st), (n / NST) & 1, w, 53))) return;
         tc_fence_after();
-        const uint64_t q_k = smem_desc_sw128(qa, 16, 1024), do_k = smem_desc_sw128(da, 16, 1024);
-        const uint64_t q_mn = smem_desc_sw128(qa, CHUNK, 1024), do_mn = smem_desc_sw128(da, CHUNK, 1024);
-        // S^T = K_j Q_i^T (the previous step's P^T was consumed by its dV products, issued earlier)
+        const uint64_t q_k = smem_desc_sw128(stage_q(st), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * CHUNK + (kk % 4) * 32;
           mma_ss(tS, desc_add(dK_kmaj, off), desc_add(q_k, off), IDESC_SD, kk > 0);
         }
-        mma_commit(BAR(S_FULL));  // P can be recomputed while dP^T is still running
-        if (D == 128 && n > 0) {  // the previous dQ^T must have left the dP^T columns
-          if (!(ok = mbar_wait(BAR(DQ_EMPTY), (n - 1) & 1, w, 54))) break;
-          tc_fence_after();
-        }
-        // dP^T = V_j dO_i^T
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * CHUNK + (kk % 4) * 32;
-          mma_ss(tDP, desc_add(dV_kmaj, off), desc_add(do_k, off), IDESC_SD, kk > 0);
-        }
-        mma_commit(BAR(DP_FULL));
-        // dV += P^T dO_i and dK += dS^T Q_i, one 32-query quarter at a time as the groups hand them over:
+        mma_commit(BAR(S_FULL));
+      };
+      if (ok) issue_s(0);
+      // Per step n the pipe runs dV(n) quarter by quarter with dP(n) after the first half,
+      // then S^T(n+1) (its P is recomputed while dK(n), dQ(n) and dP(n+1) run), then dK(n)
+      // as the dS quarters arrive, then dQ(n).  Products issued by one thread execute in
+      // order, so S^T(n+1) overwrites P^T(n) only after the dV(n) products have read it.
+      for (int n = 0; n < n_steps && ok; ++n) {
+        const int st = n % NST;
+        const uint32_t qa = stage_q(st), da = qa + L::kTile;
+        if (!(ok = mbar_wait(BAR(DO_FULL + st), (n / NST) & 1, w, 62))) break;
+        tc_fence_after();
+        const uint64_t do_k = smem_desc_sw128(da, 16, 1024);
+        const uint64_t q_mn = smem_desc_sw128(qa, CHUNK, 1024), do_mn = smem_desc_sw128(da, CHUNK, 1024);
+        // dV += P^T dO_i, one 32-query quarter at a time as the groups hand them over:
         // quarter i = group (i & 1), half (i >> 1); queries qb .. qb+31 with qb = 64*group + 32*half.
-        // P^T of a quarter arrives before its dS^T (P needs S^T only, dS also dP^T), so each half's
-        // dV products run while the groups still compute that half's dS.
 #pragma unroll
         for (int r = 0; r < 2 && ok; ++r) {
 #pragma unroll
@@ -403,17 +404,36 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
               mma_ts(tDV, tS + 64 * g + 16 * r + 8 * kk, desc_add(do_mn, rows), IDESC_KV, acc);
             }
           }
-#pragma unroll
-          for (int g = 0; g < 2 && ok; ++g) {
-            const int i = 2 * r + g, qb = 64 * g + 32 * r;
-            if (!(ok = mbar_wait(BAR(DS_READY + i), n & 1, w, 56))) break;
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-              const uint32_t acc = (n > 0 || i > 0 || kk > 0) ? 1u : 0u;
-              const uint32_t rows = (uint32_t)(qb / 16 + kk) * 2048;  // 16 query rows of Q_i
-              mma_ss(tDK, desc_add(dDS_k, g * CHUNK + (2 * r + kk) * 32), desc_add(q_mn, rows), IDESC_KV, acc);
+          if (r == 0 && ok) {
+            if (D == 128 && n > 0) {  // the previous dQ^T must have left the dP^T columns
+              if (!(ok = mbar_wait(BAR(DQ_EMPTY), (n - 1) & 1, w, 54))) break;
+              tc_fence_after();
             }
+            // dP^T = V_j dO_i^T
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk / 4) * CHUNK + (kk % 4) * 32;
+              mma_ss(tDP, desc_add(dV_kmaj, off), desc_add(do_k, off), IDESC_SD, kk > 0);
+            }
+            mma_commit(BAR(DP_FULL));
+          }
+        }
+        if (!ok) break;
+        if (n + 1 < n_steps) {
+          issue_s(n + 1);
+          if (!ok) break;
+        }
+        // dK += dS^T Q_i as the dS quarters arrive
+#pragma unroll
+        for (int i = 0; i < 4 && ok; ++i) {
+          const int r = i >> 1, g = i & 1, qb = 64 * g + 32 * r;
+          if (!(ok = mbar_wait(BAR(DS_READY + i), n & 1, w, 56))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {
+            const uint32_t acc = (n > 0 || i > 0 || kk > 0) ? 1u : 0u;
+            const uint32_t rows = (uint32_t)(qb / 16 + kk) * 2048;  // 16 query rows of Q_i
+            mma_ss(tDK, desc_add(dDS_k, g * CHUNK + (2 * r + kk) * 32), desc_add(q_mn, rows), IDESC_KV, acc);
           }
         }
         if (!ok) break;
@@ -479,8 +499,7 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
       pf = fetch(n + 1);
       // After an abort the warp keeps taking part in the named barriers and does nothing else.
       if (!ok) continue;
-      ok = mbar_wait(BAR(S_FULL), n & 1, w, 57) &&
-           (n == 0 || mbar_wait(BAR(DQ_FULL), (n - 1) & 1, w, 58));  // dS^T buffer free again
+      ok = mbar_wait(BAR(S_FULL), n & 1, w, 57);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         continue;
@@ -490,10 +509,12 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
       const bool tail_rows = k0 + 128 > it.kv_len;  // only the last key block has rows past the end
       const float sl2 = p.scale_log2, scale = p.scale;
       uint8_t* ds_row = sbase + L::kDS + g * CHUNK + kr * 128;
-#pragma unroll 1
+      // ---- P of both quarters (needs S^T only), each handed to the dV products at once.
+      // P is kept as the bf16 pairs the dV product reads until dS needs it.
+      uint32_t pp[32];
+#pragma unroll
       for (int r = 0; r < 2; ++r) {  // quarter: 32 queries
-        const uint32_t col = 64u * g + 32u * r;  // S^T / dP^T columns of the quarter
-        // ---- P (needs S^T only): handed to the dV products before dS exists
+        const uint32_t col = 64u * g + 32u * r;  // S^T columns of the quarter
         uint32_t sr[32];
         tmem_ld16(tmem + lane_off + col, sr);
         tmem_ld16(tmem + lane_off + col + 16, sr + 16);
@@ -502,14 +523,12 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
         // P = 2^(s * scale * log2 e - lse2)
         float pv[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) pv[e] = __uint_as_float(sr[e]);
-#pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) {
           const float4 nl = nl4[e4];
-          pv[4 * e4 + 0] = ex2_sfu(fmaf(pv[4 * e4 + 0], sl2, nl.x));
-          pv[4 * e4 + 1] = ex2_sfu(fmaf(pv[4 * e4 + 1], sl2, nl.y));
-          pv[4 * e4 + 2] = ex2_sfu(fmaf(pv[4 * e4 + 2], sl2, nl.z));
-          pv[4 * e4 + 3] = ex2_sfu(fmaf(pv[4 * e4 + 3], sl2, nl.w));
+          pv[4 * e4 + 0] = ex2_sfu(fmaf(__uint_as_float(sr[4 * e4 + 0]), sl2, nl.x));
+          pv[4 * e4 + 1] = ex2_sfu(fmaf(__uint_as_float(sr[4 * e4 + 1]), sl2, nl.y));
+          pv[4 * e4 + 2] = ex2_sfu(fmaf(__uint_as_float(sr[4 * e4 + 2]), sl2, nl.z));
+          pv[4 * e4 + 3] = ex2_sfu(fmaf(__uint_as_float(sr[4 * e4 + 3]), sl2, nl.w));
         }
         if (masked || (tail_rows && !row_ok)) {  // masks in a separate, warp-uniform pass
           const int q32 = qs + 32 * r;
@@ -517,47 +536,50 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
           for (int e = 0; e < 32; ++e)
             if (!row_ok || (masked && (q32 + e < ma || q32 + e > mb))) pv[e] = 0.f;
         }
-        {
-          uint32_t pp[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) pp[e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
-          // P^T over this group's already-read S^T columns: query q at column 64*(q/64) + (q%64)/2
-          tmem_st8(tmem + lane_off + 64u * g + 16u * r, pp);
-          tmem_st8(tmem + lane_off + 64u * g + 16u * r + 8u, pp + 8);
-        }
+        for (int e = 0; e < 16; ++e) pp[16 * r + e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
+        // P^T over this group's already-read S^T columns: query q at column 64*(q/64) + (q%64)/2
+        tmem_st8(tmem + lane_off + 64u * g + 16u * r, pp + 16 * r);
+        tmem_st8(tmem + lane_off + 64u * g + 16u * r + 8u, pp + 16 * r + 8);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(BAR(P_READY + 2 * r + g));
-        // ---- dS = P * (scale * dP - scale * D): needs dP^T, which lands after S^T
-        if (r == 0) {
-          ok = mbar_wait(BAR(DP_FULL), n & 1, w, 61);
-          if (!__all_sync(0xffffffffu, ok)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-        }
+      }
+      // ---- dS = P * (scale * dP - scale * D) with P as rounded for the dV product: needs dP^T,
+      // which runs after the first half's dV.
+      // Its completion also means dK and dQ of the previous step are done with the dS^T buffer.
+      ok = mbar_wait(BAR(DP_FULL), n & 1, w, 61);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        continue;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const uint32_t col = 64u * g + 32u * r;  // dP^T columns of the quarter
         uint32_t dr[32];
         tmem_ld16(tmem + lane_off + 128 + col, dr);
         tmem_ld16(tmem + lane_off + 128 + col + 16, dr + 16);
         tmem_ld_wait();
         const float4* nd4 = reinterpret_cast<const float4*>(my_dsum + 32 * r);  // -scale * D
-        uint32_t dd[16];
-#pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 nd = nd4[e4];
-          const float g0 = pv[4 * e4 + 0] * fmaf(__uint_as_float(dr[4 * e4 + 0]), scale, nd.x);
-          const float g1 = pv[4 * e4 + 1] * fmaf(__uint_as_float(dr[4 * e4 + 1]), scale, nd.y);
-          const float g2 = pv[4 * e4 + 2] * fmaf(__uint_as_float(dr[4 * e4 + 2]), scale, nd.z);
-          const float g3 = pv[4 * e4 + 3] * fmaf(__uint_as_float(dr[4 * e4 + 3]), scale, nd.w);
-          dd[2 * e4] = pack_bf16x2(g0, g1);
-          dd[2 * e4 + 1] = pack_bf16x2(g2, g3);
-        }
         // dS^T row kr, 32 queries = four 16-byte units of the 128-byte swizzled row
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          *reinterpret_cast<uint4*>(ds_row + (((4 * r + u) ^ swz) << 4)) =
-              make_uint4(dd[4 * u], dd[4 * u + 1], dd[4 * u + 2], dd[4 * u + 3]);
+        for (int u = 0; u < 4; ++u) {
+          uint32_t dd[4];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int e4 = 2 * u + h;
+            const float4 nd = nd4[e4];
+            const uint32_t p01 = pp[16 * r + 2 * e4], p23 = pp[16 * r + 2 * e4 + 1];
+            const float g0 = __uint_as_float(p01 << 16) * fmaf(__uint_as_float(dr[4 * e4 + 0]), scale, nd.x);
+            const float g1 = __uint_as_float(p01 & 0xffff0000u) * fmaf(__uint_as_float(dr[4 * e4 + 1]), scale, nd.y);
+            const float g2 = __uint_as_float(p23 << 16) * fmaf(__uint_as_float(dr[4 * e4 + 2]), scale, nd.z);
+            const float g3 = __uint_as_float(p23 & 0xffff0000u) * fmaf(__uint_as_float(dr[4 * e4 + 3]), scale, nd.w);
+            dd[2 * h] = pack_bf16x2(g0, g1);
+            dd[2 * h + 1] = pack_bf16x2(g2, g3);
+          }
+          *reinterpret_cast<uint4*>(ds_row + (((4 * r + u) ^ swz) << 4)) = make_uint4(dd[0], dd[1], dd[2], dd[3]);
+        }
         fence_proxy_async_smem();
         mbar_arrive(BAR(DS_READY + 2 * r + g));
       }
