@@ -475,28 +475,38 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
     const int swz = kr & 7;
     float* my_lse2 = s_lse2 + 64 * g;
     float* my_dsum = s_dsum + 64 * g;
-    // Thread kr < 64 carries -lse2 of query kr of the group's slice, thread
-    // kr >= 64 its -scale * D; fetched one step ahead.  Queries past the end:
-    // -lse2 = -inf (so P = 0) and D = 0.
-    auto fetch = [&](int n) -> float {
-      if (n >= n_steps) return 0.f;
-      const int qg = q_begin + (n % n_q) * 128 + 64 * g + (kr & 63);
-      const size_t row_base = row_base_of(hq_of(n));
-      if (qg >= seq_len) return kr < 64 ? -INFINITY : 0.f;
-      // staged negated, so each feeds an FMA as the addend: -lse2 and -scale * D
-      return kr < 64 ? -p.lse2[row_base + qg] : -p.scale * p.dsum[row_base + qg];
+    // Thread kr < 64 carries lse2 of query kr of the group's slice, thread
+    // kr >= 64 its D, loaded one step ahead.  The load is left raw until it
+    // is staged a step later as the FMA addends -lse2 and -scale * D, so its
+    // latency hides under a whole step.  Queries past the end: -lse2 = -inf
+    // (so P = 0) and D = 0.
+    const float* fsrc = kr < 64 ? p.lse2 : p.dsum;
+    int f_blk = 0, f_hq = h_kv * p.kv_group;  // query block and head of the next step to fetch
+    const int hq_end = f_hq + p.kv_group;
+    float f_raw = 0.f;
+    bool f_ok = false;
+    auto fetch = [&]() {
+      const int qg = q_begin + f_blk * 128 + 64 * g + (kr & 63);
+      f_ok = f_hq < hq_end && qg < seq_len;
+      f_raw = f_ok ? fsrc[row_base_of(f_hq) + qg] : 0.f;
+      if (++f_blk == n_q) {
+        f_blk = 0;
+        ++f_hq;
+      }
     };
-    float pf = fetch(0);
+    fetch();
     bool ok = true;
+    int blk = 0;  // query block of step n
     for (int n = 0; n < n_steps; ++n) {
-      const int qs = q_begin + (n % n_q) * 128 + 64 * g;  // first query of the group's slice
+      const int qs = q_begin + blk * 128 + 64 * g;  // first query of the group's slice
+      if (++blk == n_q) blk = 0;
       asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory");
       if (kr < 64)
-        my_lse2[kr] = pf;
+        my_lse2[kr] = f_ok ? -f_raw : -INFINITY;
       else
-        my_dsum[kr - 64] = pf;
+        my_dsum[kr - 64] = f_ok ? -p.scale * f_raw : 0.f;
       asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory");
-      pf = fetch(n + 1);
+      fetch();
       // After an abort the warp keeps taking part in the named barriers and does nothing else.
       if (!ok) continue;
       ok = mbar_wait(BAR(S_FULL), n & 1, w, 57);
