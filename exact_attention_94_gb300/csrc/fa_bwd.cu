@@ -47,78 +47,118 @@ __host__ __device__ __forceinline__ size_t acc_f4_index(size_t bh, int n_rows, i
     return (bh * (D / 4) + c4) * n_rows + row;
 }
 
-// One warp per row (b, h, n): D = sum_c dO * O, lse2 = lse * log2 e; the
-// dQ accumulator rows it owns are zeroed.  Tensors [Bt][rows][H][d].
+// The prologue and epilogue kernels work on tiles of 64 rows of one (batch,
+// head): O and dO rows (b, n, h) of d elements, 16 bytes per thread and four
+// rows of loads in flight, the index arithmetic done once per CTA.
+constexpr int kRowTile = 64;
+
+__device__ __forceinline__ void row_tile_of(int H, int n_rows, long long& bh, int& n0) {
+  const int n_tiles = (n_rows + kRowTile - 1) / kRowTile;
+  bh = (long long)blockIdx.x / n_tiles;
+  n0 = (int)((long long)blockIdx.x - bh * n_tiles) * kRowTile;
+}
+
+__device__ __forceinline__ float dot_bf16x8(uint4 a, uint4 b) {
+  const uint32_t ua[4] = {a.x, a.y, a.z, a.w}, ub[4] = {b.x, b.y, b.z, b.w};
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ua[i]));
+    const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ub[i]));
+    acc = fmaf(fa.x, fb.x, fmaf(fa.y, fb.y, acc));
+  }
+  return acc;
+}
+
+// Per row (b, h, n): D = sum_c dO * O and lse2 = lse * log2 e; the tile's rows
+// of the dQ accumulator are zeroed.  Tensors [Bt][rows][H][d].
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                         const __nv_bfloat16* __restrict__ dout,
                                                         const float* __restrict__ lse, float* __restrict__ dsum,
                                                         float* __restrict__ lse2, float* __restrict__ dq_acc,
-                                                        int H, int n_rows, long long total_rows) {
-  const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (gw >= total_rows) return;
-  // gw enumerates (bt, h, n) with n fastest
-  const int n = (int)(gw % n_rows);
-  const long long bh = gw / n_rows;
-  const int h = (int)(bh % H);
+                                                        int H, int n_rows) {
+  constexpr int TPR = D / 8;              // threads per row, 8 columns each
+  constexpr int RPP = 256 / TPR;          // rows per pass
+  constexpr int PASSES = kRowTile / RPP;
+  long long bh;
+  int n0;
+  row_tile_of(H, n_rows, bh, n0);
   const long long bt = bh / H;
-  const size_t base = (((size_t)bt * n_rows + n) * H + h) * D;
-  constexpr int PER = D / 32;  // elements per lane
-  float acc = 0.f;
-  if constexpr (PER == 4) {
-    const uint2 a = *reinterpret_cast<const uint2*>(o + base + lane * 4);
-    const uint2 b = *reinterpret_cast<const uint2*>(dout + base + lane * 4);
-    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+  const int h = (int)(bh - bt * H);
+  const int c8 = (int)threadIdx.x % TPR, rl = (int)threadIdx.x / TPR;
+  uint4 a[PASSES], b[PASSES];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const float2 fa = __bfloat1622float2(a2[i]);
-      const float2 fb = __bfloat1622float2(b2[i]);
-      acc = fmaf(fa.x, fb.x, fmaf(fa.y, fb.y, acc));
+  for (int k = 0; k < PASSES; ++k) {
+    const int n = n0 + rl + k * RPP;
+    a[k] = b[k] = make_uint4(0u, 0u, 0u, 0u);
+    if (n < n_rows) {
+      const size_t off = (((size_t)bt * n_rows + n) * H + h) * D + c8 * 8;
+      a[k] = *reinterpret_cast<const uint4*>(o + off);
+      b[k] = *reinterpret_cast<const uint4*>(dout + off);
     }
-  } else {
-    const uint32_t a = *reinterpret_cast<const uint32_t*>(o + base + lane * 2);
-    const uint32_t b = *reinterpret_cast<const uint32_t*>(dout + base + lane * 2);
-    const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a));
-    const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b));
-    acc = fmaf(fa.x, fb.x, fa.y * fb.y);
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  const size_t ri = (size_t)bh * n_rows + n;
-  if (lane == 0) {
-    dsum[ri] = acc;
-    lse2[ri] = lse[ri] * 1.4426950408889634f;
+  for (int k = 0; k < PASSES; ++k) {
+    float acc = dot_bf16x8(a[k], b[k]);
+#pragma unroll
+    for (int w = TPR / 2; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
+    const int n = n0 + rl + k * RPP;
+    if (c8 == 0 && n < n_rows) {
+      const size_t ri = (size_t)bh * n_rows + n;
+      dsum[ri] = acc;
+      lse2[ri] = lse[ri] * 1.4426950408889634f;
+    }
   }
-  // zero this row of the accumulator: d/4 groups of 4 floats
-  if (lane < D / 4) {
-    float4* dst = reinterpret_cast<float4*>(dq_acc) + acc_f4_index<D>((size_t)bh, n_rows, n, lane);
-    *dst = make_float4(0.f, 0.f, 0.f, 0.f);
+  // zero the tile's accumulator rows: 64 rows x d/4 groups of 4 floats
+  float4* acc4 = reinterpret_cast<float4*>(dq_acc);
+#pragma unroll
+  for (int k = 0; k < kRowTile * (D / 4) / 256; ++k) {
+    const int i = (int)threadIdx.x + 256 * k;
+    // d = 128: row-major tile, a row's 32 groups contiguous; d = 64: 16 planes of 64 rows
+    const int row = D == 128 ? i / (D / 4) : i % kRowTile;
+    const int c4 = D == 128 ? i % (D / 4) : i / kRowTile;
+    if (n0 + row < n_rows) acc4[acc_f4_index<D>((size_t)bh, n_rows, n0 + row, c4)] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
 
-// dq[bt][n][h][c] = bf16(acc[bt*H+h][c/4][n][c%4]); one thread per 4 columns of a row.
+// dq[bt][n][h][c] = bf16(dQ accumulator), 8 columns per thread.
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_post_kernel(const float* __restrict__ dq_acc,
-                                                         __nv_bfloat16* __restrict__ dq, int H, int n_rows,
-                                                         long long total) {
-  const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= total) return;
-  // t enumerates (bt, n, h, c4) with c4 fastest: coalesced bf16 writes
-  constexpr int G = D / 4;
-  const int c4 = (int)(t % G);
-  long long r = t / G;
-  const int h = (int)(r % H);
-  r /= H;
-  const int n = (int)(r % n_rows);
-  const long long bt = r / n_rows;
-  const long long bh = bt * H + h;
-  const float4 v = reinterpret_cast<const float4*>(dq_acc)[acc_f4_index<D>((size_t)bh, n_rows, n, c4)];
-  uint2 out;
-  out.x = pack_bf16x2(v.x, v.y);
-  out.y = pack_bf16x2(v.z, v.w);
-  *reinterpret_cast<uint2*>(dq + (((size_t)bt * n_rows + n) * H + h) * D + c4 * 4) = out;
+                                                         __nv_bfloat16* __restrict__ dq, int H, int n_rows) {
+  constexpr int TPR = D / 8;
+  constexpr int RPP = 256 / TPR;
+  constexpr int PASSES = kRowTile / RPP;
+  long long bh;
+  int n0;
+  row_tile_of(H, n_rows, bh, n0);
+  const long long bt = bh / H;
+  const int h = (int)(bh - bt * H);
+  // d = 128: a row's 16 threads read 512 contiguous accumulator bytes; d = 64: the
+  // threads of a warp take 32 consecutive rows of one column pair (512 contiguous bytes
+  // per plane of the [B*H][d/4][rows][4] layout)
+  const int c8 = D == 128 ? (int)threadIdx.x % TPR : (int)threadIdx.x / RPP;
+  const int rl = D == 128 ? (int)threadIdx.x / TPR : (int)threadIdx.x % RPP;
+  const float4* acc4 = reinterpret_cast<const float4*>(dq_acc);
+  float4 v0[PASSES], v1[PASSES];
+#pragma unroll
+  for (int k = 0; k < PASSES; ++k) {
+    const int n = n0 + rl + k * RPP;
+    v0[k] = v1[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (n < n_rows) {
+      v0[k] = acc4[acc_f4_index<D>((size_t)bh, n_rows, n, 2 * c8)];
+      v1[k] = acc4[acc_f4_index<D>((size_t)bh, n_rows, n, 2 * c8 + 1)];
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < PASSES; ++k) {
+    const int n = n0 + rl + k * RPP;
+    if (n < n_rows) {
+      const uint4 out = make_uint4(pack_bf16x2(v0[k].x, v0[k].y), pack_bf16x2(v0[k].z, v0[k].w),
+                                   pack_bf16x2(v1[k].x, v1[k].y), pack_bf16x2(v1[k].z, v1[k].w));
+      *reinterpret_cast<uint4*>(dq + (((size_t)bt * n_rows + n) * H + h) * D + c8 * 8) = out;
+    }
+  }
 }
 
 // ---------------------------------------------------------------- work items and masks
@@ -690,10 +730,12 @@ static auto main_kernel_for() {
 template <int D, int MASK>
 static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream) {
-  const long long rows = (long long)p.B_tensor * p.H * p.n_rows;
-  fa_bwd_pre_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
+  // row tiles: one CTA per (batch, head) and 64 rows
+  const long long tiles = (long long)p.B_tensor * p.H * ((p.n_rows + kRowTile - 1) / kRowTile);
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+  fa_bwd_pre_kernel<D><<<(unsigned)tiles, 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(p.o), static_cast<const __nv_bfloat16*>(p.dout), p.lse, p.dsum, p.lse2,
-      p.dq_acc, p.H, p.n_rows, rows);
+      p.dq_acc, p.H, p.n_rows);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
@@ -714,9 +756,8 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
-  const long long total = rows * (D / 4);
-  fa_bwd_post_kernel<D><<<(unsigned)((total + 255) / 256), 256, 0, stream>>>(
-      p.dq_acc, static_cast<__nv_bfloat16*>(p.dq), p.H, p.n_rows, total);
+  fa_bwd_post_kernel<D><<<(unsigned)tiles, 256, 0, stream>>>(p.dq_acc, static_cast<__nv_bfloat16*>(p.dq), p.H,
+                                                             p.n_rows);
   return cudaGetLastError();
 }
 
