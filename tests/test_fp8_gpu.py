@@ -21,7 +21,7 @@ import torch
 
 import oracle
 import synth
-from exact_attention_94_gb300 import ops
+from exact_attention_94_gb300 import _lib, ops
 from oracle import fp8 as F
 from tests.parity import assert_lse
 
@@ -119,6 +119,19 @@ def test_fp8_forward_statistical(case):
     qh, kh, vh, vs, eff, o_ref, l_ref = _reference(x, signs, wl, wr, 1.0 / math.sqrt(d))
     assert_lse(lse.cpu().numpy(), l_ref, f"fp8 lse {case}")
     _check_stat(o, o_ref, _sigma(qh, kh, vh, vs, eff, wl, wr), f"fp8 O {case}")
+
+
+@pytest.mark.parametrize("tau", [0.0, 30.0])
+def test_fp8_forward_rescale_threshold(tau):
+    """Threshold 0 moves a row's reference whenever its maximum grows (each such
+    key tile is worked again with the new reference); 30 almost never does.  The
+    result is the same attention either way."""
+    ops.set_option(_lib.FA_OPT_RESCALE_TAU, tau)
+    try:
+        test_fp8_forward_statistical((1, 640, 640, 2, 2, 100, 0, True))
+        test_fp8_forward_statistical((2, 300, 300, 4, 2, -1, 0, True))
+    finally:
+        ops.set_option(_lib.FA_OPT_RESCALE_TAU, 8.0)
 
 
 @pytest.mark.parametrize("causal", [False, True])

@@ -16,11 +16,12 @@ pytestmark = pytest.mark.gpu
 def _built():
     from exact_attention_94_gb300 import build
     build.build()
+    # the library's defaults: threshold 8, every exponential on the SFU
     ops.set_option(_lib.FA_OPT_RESCALE_TAU, 8.0)
-    ops.set_option(_lib.FA_OPT_POLY_EXP, 1)
+    ops.set_option(_lib.FA_OPT_POLY_EXP, 0)
     yield
     ops.set_option(_lib.FA_OPT_RESCALE_TAU, 8.0)
-    ops.set_option(_lib.FA_OPT_POLY_EXP, 1)
+    ops.set_option(_lib.FA_OPT_POLY_EXP, 0)
 
 
 def run_dense(B, H, N, d, causal, seed=0, k_boost=1.0):
@@ -69,7 +70,7 @@ def test_rescale_threshold_and_exp_split(tau, poly):
         check_dense(1, 4, 1024, 128, True, seed=3, k_boost=3.0)
     finally:
         ops.set_option(_lib.FA_OPT_RESCALE_TAU, 8.0)
-        ops.set_option(_lib.FA_OPT_POLY_EXP, 1)
+        ops.set_option(_lib.FA_OPT_POLY_EXP, 0)
 
 
 def test_large_score_offsets():
