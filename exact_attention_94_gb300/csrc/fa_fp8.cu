@@ -9,7 +9,8 @@
 //   rotate:   x <- (x H) * signs, H the Sylvester-Hadamard matrix (entries
 //             +-1), by the fast transform: stage widths 1, 2, 4, ..., d/2, each
 //             butterfly (a, b) -> (a + b, a - b) in fp32.  Widths below 16
-//             stay inside a lane, the others pair lanes with shuffles.
+//             stay inside a lane, the others pair lanes with shuffles.  The
+//             signs are applied in the final multiply by the inverse scale.
 //   scale:    amax / 448 over the block (fp32, correctly rounded); 0 for an
 //             all-zero block, whose codes are 0.
 //   codes:    e4m3(x * (1 / scale)), the reciprocal and the product each
@@ -44,13 +45,15 @@ __device__ __forceinline__ void fwht_row16(float (&v)[kElems], int lane) {
       }
     }
   }
+  // the lower lane of a pair keeps a + b, the upper one a - b: one FMA with a
+  // +-1 multiplier, rounded once exactly like the add or subtract it replaces
 #pragma unroll
   for (int hl = 1; hl < LPR; hl <<= 1) {
-    const bool upper = (lane & hl) != 0;
+    const float sg = (lane & hl) ? -1.f : 1.f;
 #pragma unroll
     for (int i = 0; i < kElems; ++i) {
       const float o = __shfl_xor_sync(0xffffffffu, v[i], hl);
-      v[i] = upper ? (o - v[i]) : (v[i] + o);
+      v[i] = fmaf(v[i], sg, o);
     }
   }
 }
@@ -98,14 +101,9 @@ __global__ void __launch_bounds__(kQuantThreads) fa_fp8_quant_kernel(const __nv_
 #pragma unroll
       for (int e = 0; e < kElems; ++e) v[it][e] = 0.f;
     }
-    if (ROT) {
-      fwht_row16<LPR>(v[it], lane);
+    if (ROT) fwht_row16<LPR>(v[it], lane);  // the signs come with the scale below
 #pragma unroll
-      for (int e = 0; e < kElems; ++e)  // times -1: flip the sign bit
-        v[it][e] = __uint_as_float(__float_as_uint(v[it][e]) ^ (((neg >> e) & 1u) << 31));
-    }
-#pragma unroll
-    for (int e = 0; e < kElems; ++e) amax = fmaxf(amax, fabsf(v[it][e]));
+    for (int e = 0; e < kElems; e += 2) amax = max3f(amax, fabsf(v[it][e]), fabsf(v[it][e + 1]));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -117,6 +115,11 @@ __global__ void __launch_bounds__(kQuantThreads) fa_fp8_quant_kernel(const __nv_
   const float scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 0.f;
   const float inv = amax > 0.f ? __frcp_rn(scale) : 0.f;  // codes = e4m3(x * (1 / scale))
   if (threadIdx.x == 0) scales[((size_t)b * H + h) * nblk + blk] = scale;
+  // x * sign * (1 / scale) as x * (sign * (1 / scale)): the sign is exact and
+  // round-to-nearest is symmetric, so each code (and each zero's sign) is the same
+  float sinv[kElems];
+#pragma unroll
+  for (int e = 0; e < kElems; ++e) sinv[e] = ((neg >> e) & 1u) ? -inv : inv;
 
 #pragma unroll
   for (int it = 0; it < IT; ++it) {
@@ -125,8 +128,8 @@ __global__ void __launch_bounds__(kQuantThreads) fa_fp8_quant_kernel(const __nv_
     uint32_t wd[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q)
-      wd[q] = pack_e4m3x4(__fmul_rn(v[it][4 * q], inv), __fmul_rn(v[it][4 * q + 1], inv),
-                          __fmul_rn(v[it][4 * q + 2], inv), __fmul_rn(v[it][4 * q + 3], inv));
+      wd[q] = pack_e4m3x4(__fmul_rn(v[it][4 * q], sinv[4 * q]), __fmul_rn(v[it][4 * q + 1], sinv[4 * q + 1]),
+                          __fmul_rn(v[it][4 * q + 2], sinv[4 * q + 2]), __fmul_rn(v[it][4 * q + 3], sinv[4 * q + 3]));
     uint4 word = make_uint4(wd[0], wd[1], wd[2], wd[3]);
     if (!(amax > 0.f)) word = make_uint4(0u, 0u, 0u, 0u);  // all-zero block: +0 codes (not -0 from flipped zeros)
     if constexpr (TR) {
