@@ -340,7 +340,7 @@ def run_e2e(args, ctx):
         torch.cuda.synchronize()
 
     run(3)
-    steps = max(4, args.steps // 2)
+    steps = max(4, args.steps)  # the pipeline's fill and drain (one step's copies each) spread over as many steps
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     run(steps, start, end)
