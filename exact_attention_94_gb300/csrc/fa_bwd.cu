@@ -389,7 +389,8 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
     }
   } else if (warp == kWarpMma) {
     // ============================================================ MMA issuer
-    if (lane == 0) {
+    // the whole warp runs the loop; one elected lane issues each product and commit
+    {
       constexpr uint32_t IDESC_SD = idesc_bf16(128, 128, false, false);  // S^T, dP^T: M keys, N queries
       constexpr uint32_t IDESC_KV = idesc_bf16(128, D, false, true);     // dV, dK: M keys, N d
       // d = 128: dQ^T, M d, N queries, both operands MN-major; d = 64: dQ, M queries, N d, both MN-major
@@ -401,20 +402,20 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
       const uint64_t dK_mn = smem_desc_sw128(sK, CHUNK, 1024);   // K_j^T as MN-major A over d
       const uint64_t dDS_k = smem_desc_sw128(sDS, 16, 1024);     // dS^T as K-major A (rows = keys)
       const uint64_t dDS_mn = smem_desc_sw128(sDS, CHUNK, 1024); // dS^T as MN-major B over queries
-      bool ok = mbar_wait(BAR(KV_FULL), 0, w, 52);
+      bool ok = __all_sync(0xffffffffu, mbar_wait(BAR(KV_FULL), 0, w, 52));
       tc_fence_after();
       // S^T(n) = K_j Q_n^T into columns [0,128)
       auto issue_s = [&](int n) {
         const int st = n % NST;
-        if (!(ok = mbar_wait(BAR(Q_FULL + st), (n / NST) & 1, w, 53))) return;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(Q_FULL + st), (n / NST) & 1, w, 53)))) return;
         tc_fence_after();
         const uint64_t q_k = smem_desc_sw128(stage_q(st), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * CHUNK + (kk % 4) * 32;
-          mma_ss(tS, desc_add(dK_kmaj, off), desc_add(q_k, off), IDESC_SD, kk > 0);
+          mma_ss_w(tS, desc_add(dK_kmaj, off), desc_add(q_k, off), IDESC_SD, kk > 0);
         }
-        mma_commit(BAR(S_FULL));
+        mma_commit_w(BAR(S_FULL));
       };
       if (ok) issue_s(0);
       // Per step n the pipe runs dV(n) quarter by quarter with dP(n) after the first half,
@@ -424,7 +425,7 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
       for (int n = 0; n < n_steps && ok; ++n) {
         const int st = n % NST;
         const uint32_t qa = stage_q(st), da = qa + L::kTile;
-        if (!(ok = mbar_wait(BAR(DO_FULL + st), (n / NST) & 1, w, 62))) break;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(DO_FULL + st), (n / NST) & 1, w, 62)))) break;
         tc_fence_after();
         const uint64_t do_k = smem_desc_sw128(da, 16, 1024);
         const uint64_t q_mn = smem_desc_sw128(qa, CHUNK, 1024), do_mn = smem_desc_sw128(da, CHUNK, 1024);
@@ -435,27 +436,27 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
 #pragma unroll
           for (int g = 0; g < 2; ++g) {
             const int i = 2 * r + g, qb = 64 * g + 32 * r;
-            if (!(ok = mbar_wait(BAR(P_READY + i), n & 1, w, 55))) break;
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(P_READY + i), n & 1, w, 55)))) break;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
               const uint32_t acc = (n > 0 || i > 0 || kk > 0) ? 1u : 0u;
               const uint32_t rows = (uint32_t)(qb / 16 + kk) * 2048;  // 16 query rows of dO_i
-              mma_ts(tDV, tS + 64 * g + 16 * r + 8 * kk, desc_add(do_mn, rows), IDESC_KV, acc);
+              mma_ts_w(tDV, tS + 64 * g + 16 * r + 8 * kk, desc_add(do_mn, rows), IDESC_KV, acc);
             }
           }
           if (r == 0 && ok) {
             if (D == 128 && n > 0) {  // the previous dQ^T must have left the dP^T columns
-              if (!(ok = mbar_wait(BAR(DQ_EMPTY), (n - 1) & 1, w, 54))) break;
+              if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(DQ_EMPTY), (n - 1) & 1, w, 54)))) break;
               tc_fence_after();
             }
             // dP^T = V_j dO_i^T
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (kk / 4) * CHUNK + (kk % 4) * 32;
-              mma_ss(tDP, desc_add(dV_kmaj, off), desc_add(do_k, off), IDESC_SD, kk > 0);
+              mma_ss_w(tDP, desc_add(dV_kmaj, off), desc_add(do_k, off), IDESC_SD, kk > 0);
             }
-            mma_commit(BAR(DP_FULL));
+            mma_commit_w(BAR(DP_FULL));
           }
         }
         if (!ok) break;
@@ -467,38 +468,38 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
 #pragma unroll
         for (int i = 0; i < 4 && ok; ++i) {
           const int r = i >> 1, g = i & 1, qb = 64 * g + 32 * r;
-          if (!(ok = mbar_wait(BAR(DS_READY + i), n & 1, w, 56))) break;
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(DS_READY + i), n & 1, w, 56)))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk) {
             const uint32_t acc = (n > 0 || i > 0 || kk > 0) ? 1u : 0u;
             const uint32_t rows = (uint32_t)(qb / 16 + kk) * 2048;  // 16 query rows of Q_i
-            mma_ss(tDK, desc_add(dDS_k, g * CHUNK + (2 * r + kk) * 32), desc_add(q_mn, rows), IDESC_KV, acc);
+            mma_ss_w(tDK, desc_add(dDS_k, g * CHUNK + (2 * r + kk) * 32), desc_add(q_mn, rows), IDESC_KV, acc);
           }
         }
         if (!ok) break;
-        mma_commit(BAR(STAGE_EMPTY + st));
+        mma_commit_w(BAR(STAGE_EMPTY + st));
         if constexpr (D == 128) {
           // dQ^T = K_j^T dS^T (M = d, N = 128 queries over both dS^T chunks, K = 128 keys) into the dP^T columns
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tDP, desc_add(dK_mn, kk * 2048), desc_add(dDS_mn, kk * 2048), IDESC_DQ, kk > 0);
+            mma_ss_w(tDP, desc_add(dK_mn, kk * 2048), desc_add(dDS_mn, kk * 2048), IDESC_DQ, kk > 0);
         } else {
           // dQ = dS K_j (M = 128 queries, N = d, K = 128 keys): A is dS^T read MN-major over the
           // queries, B is K_j read MN-major over d; its own columns, free once the previous one is drained
           if (n > 0) {
-            if (!(ok = mbar_wait(BAR(DQ_EMPTY), (n - 1) & 1, w, 54))) break;
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(DQ_EMPTY), (n - 1) & 1, w, 54)))) break;
             tc_fence_after();
           }
           constexpr uint32_t IDESC_DQ64 = idesc_bf16(128, D, true, true);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tDQ, desc_add(dDS_mn, kk * 2048), desc_add(dK_mn, kk * 2048), IDESC_DQ64, kk > 0);
+            mma_ss_w(tDQ, desc_add(dDS_mn, kk * 2048), desc_add(dK_mn, kk * 2048), IDESC_DQ64, kk > 0);
         }
-        mma_commit(BAR(DQ_FULL));
+        mma_commit_w(BAR(DQ_FULL));
       }
-      if (ok) mma_commit(BAR(DKV_FINAL));
-      mma_commit(BAR(DRAIN));
+      if (ok) mma_commit_w(BAR(DKV_FINAL));
+      mma_commit_w(BAR(DRAIN));
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(BAR(DRAIN), 0) && globaltimer_ns() - t0 < p.timeout_ns) {
       }

@@ -170,6 +170,31 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// The issuing warp runs its loop with every lane (uniform control flow, so the
+// operands stay warp-uniform) and one lane, picked by elect.sync, issues each
+// tcgen05 instruction.  Issued from a lone lane inside a divergent branch a
+// product measured twice as long to issue (123 against 64 cycles for M = N = 128).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+__device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t acc) {
+  if (elect_one()) mma_ss(d_tmem, a_desc, b_desc, idesc, acc);
+}
+__device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t acc) {
+  if (elect_one()) mma_ts(d_tmem, a_tmem, b_desc, idesc, acc);
+}
+__device__ __forceinline__ void mma_commit_w(uint32_t bar) {
+  if (elect_one()) mma_commit(bar);
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle, tcgen05 version bits.
 // start address, leading-dimension byte offset and stride-dimension byte
 // offset are stored in 16-byte units.
