@@ -203,7 +203,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ============================================================ MMA issuer
-    if (lane == 0) {
+    // the whole warp runs the loop; one elected lane issues each product and commit
+    {
       constexpr uint32_t IDESC_S = F8 ? idesc_e4m3(128, 128) : idesc_bf16(128, 128, false, false);
       constexpr uint32_t IDESC_O = F8 ? idesc_e4m3(128, D) : idesc_bf16(128, D, false, true);
       const uint32_t tS0 = tmem, tS1 = tmem + 128;
@@ -219,9 +220,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < (int)(D * L::kElt / 32); ++kk) {
           const uint32_t off = (kk / 4) * CHUNK + (kk % 4) * 32;
           if constexpr (F8)
-            mma_ss_f8(dst, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024), IDESC_S, kk > 0);
+            mma_ss_f8_w(dst, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024), IDESC_S, kk > 0);
           else
-            mma_ss(dst, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024), IDESC_S, kk > 0);
+            mma_ss_w(dst, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024), IDESC_S, kk > 0);
         }
       };
       // O_t += P_t V with P from TMEM over S_t's columns.  bf16: pairs per column,
@@ -233,67 +234,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (F8) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts_f8(dst, pa + kk * 8, smem_desc_sw128(va + kk * 32, 16, 1024), IDESC_O, (acc || kk > 0) ? 1u : 0u);
+            mma_ts_f8_w(dst, pa + kk * 8, smem_desc_sw128(va + kk * 32, 16, 1024), IDESC_O, (acc || kk > 0) ? 1u : 0u);
         } else {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ts(dst, pa + kk * 8, smem_desc_sw128(va + kk * 2048, CHUNK, 1024), IDESC_O,
+            mma_ts_w(dst, pa + kk * 8, smem_desc_sw128(va + kk * 2048, CHUNK, 1024), IDESC_O,
                    (acc || kk > 0) ? 1u : 0u);
         }
       };
 
-      ok = mbar_wait(BAR(Q_FULL), 0, w, 2);
+      ok = __all_sync(0xffffffffu, mbar_wait(BAR(Q_FULL), 0, w, 2));
       tc_fence_after();
       // Ring position u of key tile j is 2 (j - jmin) (K) and 2 (j - jmin) + 1 (V);
       // tile t's S / P barriers complete once per visited key tile, phase j - jlo_t.
       for (int j = jmin; j < jmax && ok; ++j) {
         const int uk = 2 * (j - jmin), sk = uk % NS;
-        if (!(ok = mbar_wait(BAR(KV_FULL + sk), (uk / NS) & 1, w, 3))) break;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(KV_FULL + sk), (uk / NS) & 1, w, 3)))) break;
         tc_fence_after();
         if (j >= jlo0 && j < jhi0) {
           issue_S(0, sk);
-          mma_commit(BAR(S_FULL + 0));
+          mma_commit_w(BAR(S_FULL + 0));
         }
         if (j > jmin) {
           const int sv = (uk - 1) % NS;
           if (j - 1 >= jlo1 && j - 1 < jhi1) {
-            if (!(ok = mbar_wait(BAR(P_FULL + 1), (j - 1 - jlo1) & 1, w, 4))) break;
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(P_FULL + 1), (j - 1 - jlo1) & 1, w, 4)))) break;
             tc_fence_after();
             issue_PV(1, sv, j - 1 > jlo1);
-            if (j - 1 == jhi1 - 1) mma_commit(BAR(O_FINAL + 1));
+            if (j - 1 == jhi1 - 1) mma_commit_w(BAR(O_FINAL + 1));
           }
-          mma_commit(BAR(KV_EMPTY + sv));
+          mma_commit_w(BAR(KV_EMPTY + sv));
         }
         if (j >= jlo1 && j < jhi1) {
           issue_S(1, sk);
-          mma_commit(BAR(S_FULL + 1));
+          mma_commit_w(BAR(S_FULL + 1));
         }
-        mma_commit(BAR(KV_EMPTY + sk));
+        mma_commit_w(BAR(KV_EMPTY + sk));
         const int uv = uk + 1, sv = uv % NS;
-        if (!(ok = mbar_wait(BAR(KV_FULL + sv), (uv / NS) & 1, w, 5))) break;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(KV_FULL + sv), (uv / NS) & 1, w, 5)))) break;
         tc_fence_after();
         if (j >= jlo0 && j < jhi0) {
-          if (!(ok = mbar_wait(BAR(P_FULL + 0), (j - jlo0) & 1, w, 6))) break;
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(P_FULL + 0), (j - jlo0) & 1, w, 6)))) break;
           tc_fence_after();
           issue_PV(0, sv, j > jlo0);
-          if (j == jhi0 - 1) mma_commit(BAR(O_FINAL + 0));
+          if (j == jhi0 - 1) mma_commit_w(BAR(O_FINAL + 0));
         }
       }
       if (ok && jmax > jmin) {
         const int j = jmax;
         const int sv = (2 * (j - 1 - jmin) + 1) % NS;
         if (j - 1 >= jlo1 && j - 1 < jhi1) {
-          if ((ok = mbar_wait(BAR(P_FULL + 1), (j - 1 - jlo1) & 1, w, 4))) {
+          if ((ok = __all_sync(0xffffffffu, mbar_wait(BAR(P_FULL + 1), (j - 1 - jlo1) & 1, w, 4)))) {
             tc_fence_after();
             issue_PV(1, sv, j - 1 > jlo1);
-            mma_commit(BAR(O_FINAL + 1));
+            mma_commit_w(BAR(O_FINAL + 1));
           }
         }
-        if (ok) mma_commit(BAR(KV_EMPTY + sv));
+        if (ok) mma_commit_w(BAR(KV_EMPTY + sv));
       }
       // Drain: every product and every earlier commit's arrival has landed
       // before TMEM is released and the CTA's shared memory goes away.
-      mma_commit(BAR(DRAIN));
+      mma_commit_w(BAR(DRAIN));
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(BAR(DRAIN), 0) && globaltimer_ns() - t0 < p.timeout_ns) {
       }

@@ -194,6 +194,14 @@ __device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint6
 __device__ __forceinline__ void mma_commit_w(uint32_t bar) {
   if (elect_one()) mma_commit(bar);
 }
+__device__ __forceinline__ void mma_ss_f8_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t acc) {
+  if (elect_one()) mma_ss_f8(d_tmem, a_desc, b_desc, idesc, acc);
+}
+__device__ __forceinline__ void mma_ts_f8_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t acc) {
+  if (elect_one()) mma_ts_f8(d_tmem, a_tmem, b_desc, idesc, acc);
+}
 
 // Shared-memory matrix descriptor, 128-byte swizzle, tcgen05 version bits.
 // start address, leading-dimension byte offset and stride-dimension byte
