@@ -357,29 +357,36 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
 
   if (warp == kWarpProducer) {
     // ============================================================ TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      tma_prefetch_desc(&tm_do);
-      mbar_arrive_expect_tx(BAR(KV_FULL), 2 * L::kTile);
-      for (int c = 0; c < CH; ++c) {
-        tma_load_4d(sK + c * CHUNK, &tm_k, BAR(KV_FULL), c * 64, kv_start + k0, h_kv, b_coord);
-        tma_load_4d(sV + c * CHUNK, &tm_v, BAR(KV_FULL), c * 64, kv_start + k0, h_kv, b_coord);
+    // the whole warp runs the loop; one elected lane issues the copies
+    {
+      if (elect_one()) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        tma_prefetch_desc(&tm_do);
+        mbar_arrive_expect_tx(BAR(KV_FULL), 2 * L::kTile);
+        for (int c = 0; c < CH; ++c) {
+          tma_load_4d(sK + c * CHUNK, &tm_k, BAR(KV_FULL), c * 64, kv_start + k0, h_kv, b_coord);
+          tma_load_4d(sV + c * CHUNK, &tm_v, BAR(KV_FULL), c * 64, kv_start + k0, h_kv, b_coord);
+        }
       }
       bool ok = true;
       for (int n = 0; n < n_steps && ok; ++n) {
         const int st = n % NST;
         const int row = seq_start + q_begin + (n % n_q) * 128;
         const int hq = hq_of(n);
-        if (n >= NST && !(ok = mbar_wait(BAR(STAGE_EMPTY + st), ((n / NST) - 1) & 1, w, 51))) break;
+        if (n >= NST &&
+            !(ok = __all_sync(0xffffffffu, mbar_wait(BAR(STAGE_EMPTY + st), ((n / NST) - 1) & 1, w, 51))))
+          break;
         const uint32_t qa = stage_q(st);
         // Q_i first: S^T of a step is issued while the previous step's products still run
-        mbar_arrive_expect_tx(BAR(Q_FULL + st), L::kTile);
-        for (int c = 0; c < CH; ++c) tma_load_4d(qa + c * CHUNK, &tm_q, BAR(Q_FULL + st), c * 64, row, hq, b_coord);
-        mbar_arrive_expect_tx(BAR(DO_FULL + st), L::kTile);
-        for (int c = 0; c < CH; ++c)
-          tma_load_4d(qa + L::kTile + c * CHUNK, &tm_do, BAR(DO_FULL + st), c * 64, row, hq, b_coord);
+        if (elect_one()) {
+          mbar_arrive_expect_tx(BAR(Q_FULL + st), L::kTile);
+          for (int c = 0; c < CH; ++c) tma_load_4d(qa + c * CHUNK, &tm_q, BAR(Q_FULL + st), c * 64, row, hq, b_coord);
+          mbar_arrive_expect_tx(BAR(DO_FULL + st), L::kTile);
+          for (int c = 0; c < CH; ++c)
+            tma_load_4d(qa + L::kTile + c * CHUNK, &tm_do, BAR(DO_FULL + st), c * 64, row, hq, b_coord);
+        }
       }
       if (!ok) {
         const uint64_t t0 = globaltimer_ns();
