@@ -248,7 +248,8 @@ __device__ void bwd_zero_dkdv(const BwdParams& p, const BwdItem& it, int Hkv, in
 //           three for d = 64); dS^T 128 keys x 128 queries (two 64-query chunks).
 // Warps: 0-3 and 12-15 drain dQ (d = 128: query columns 0-63 and 64-127 of
 // dQ^T; d = 64: d columns 0-31 and 32-63 of dQ), 4-11 recompute P and dS,
-// 16 issues TMA loads, 17 owns TMEM and issues the MMAs.
+// 16 issues TMA loads and 17 owns TMEM and issues the MMAs (each warp runs its
+// loop with all lanes; an elect.sync lane issues each copy or product).
 constexpr int kBwd128Threads = 576;
 constexpr int kWarpProducer = 16;
 constexpr int kWarpMma = 17;

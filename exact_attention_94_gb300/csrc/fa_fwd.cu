@@ -25,7 +25,7 @@
 //
 // CTA organisation (one CTA per pair of 128-row query tiles of one head):
 //   warp 0      TMA producer: Q tiles once, then K_j, V_j into a ring of slots
-//   warp 1      allocates TMEM; one lane issues every tcgen05.mma
+//   warp 1      allocates TMEM and runs the MMA loop; an elect.sync lane issues each tcgen05.mma
 //   warps 4-7   softmax of query tile 0 (thread = row = TMEM lane)
 //   warps 8-11  softmax of query tile 1
 // The tensor pipe alternates between the two tiles (S0_j, PV1_{j-1}, S1_j,
