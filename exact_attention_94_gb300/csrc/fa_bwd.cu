@@ -567,6 +567,7 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
       const bool masked = mask_needed<MASK>(p, it, k0, qs, 64);
       const bool tail_rows = k0 + 128 > it.kv_len;  // only the last key block has rows past the end
       const float sl2 = p.scale_log2, scale = p.scale;
+      const uint64_t sl2x2 = f2_pack(sl2, sl2), scale2 = f2_pack(scale, scale);
       uint8_t* ds_row = sbase + L::kDS + g * CHUNK + kr * 128;
       // ---- P of both quarters (needs S^T only), each handed to the dV products at once.
       // P is kept as the bf16 pairs the dV product reads until dS needs it.
@@ -584,10 +585,16 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) {
           const float4 nl = nl4[e4];
-          pv[4 * e4 + 0] = ex2_sfu(fmaf(__uint_as_float(sr[4 * e4 + 0]), sl2, nl.x));
-          pv[4 * e4 + 1] = ex2_sfu(fmaf(__uint_as_float(sr[4 * e4 + 1]), sl2, nl.y));
-          pv[4 * e4 + 2] = ex2_sfu(fmaf(__uint_as_float(sr[4 * e4 + 2]), sl2, nl.z));
-          pv[4 * e4 + 3] = ex2_sfu(fmaf(__uint_as_float(sr[4 * e4 + 3]), sl2, nl.w));
+          // packed f32x2 FMAs: the same fused results as the scalar ones
+          float y0, y1, y2, y3;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * e4 + 0]), __uint_as_float(sr[4 * e4 + 1])), sl2x2,
+                           f2_pack(nl.x, nl.y)), y0, y1);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * e4 + 2]), __uint_as_float(sr[4 * e4 + 3])), sl2x2,
+                           f2_pack(nl.z, nl.w)), y2, y3);
+          pv[4 * e4 + 0] = ex2_sfu(y0);
+          pv[4 * e4 + 1] = ex2_sfu(y1);
+          pv[4 * e4 + 2] = ex2_sfu(y2);
+          pv[4 * e4 + 3] = ex2_sfu(y3);
         }
         if (masked || (tail_rows && !row_ok)) {  // masks in a separate, warp-uniform pass
           const int q32 = qs + 32 * r;
@@ -630,10 +637,14 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
             const int e4 = 2 * u + h;
             const float4 nd = nd4[e4];
             const uint32_t p01 = pp[16 * r + 2 * e4], p23 = pp[16 * r + 2 * e4 + 1];
-            const float g0 = __uint_as_float(p01 << 16) * fmaf(__uint_as_float(dr[4 * e4 + 0]), scale, nd.x);
-            const float g1 = __uint_as_float(p01 & 0xffff0000u) * fmaf(__uint_as_float(dr[4 * e4 + 1]), scale, nd.y);
-            const float g2 = __uint_as_float(p23 << 16) * fmaf(__uint_as_float(dr[4 * e4 + 2]), scale, nd.z);
-            const float g3 = __uint_as_float(p23 & 0xffff0000u) * fmaf(__uint_as_float(dr[4 * e4 + 3]), scale, nd.w);
+            // packed f32x2: (scale * dP - scale * D) then times P, the same results as scalar
+            float g0, g1, g2, g3;
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(p01 << 16), __uint_as_float(p01 & 0xffff0000u)),
+                             f2_fma(f2_pack(__uint_as_float(dr[4 * e4 + 0]), __uint_as_float(dr[4 * e4 + 1])), scale2,
+                                    f2_pack(nd.x, nd.y))), g0, g1);
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(p23 << 16), __uint_as_float(p23 & 0xffff0000u)),
+                             f2_fma(f2_pack(__uint_as_float(dr[4 * e4 + 2]), __uint_as_float(dr[4 * e4 + 3])), scale2,
+                                    f2_pack(nd.z, nd.w))), g2, g3);
             dd[2 * h] = pack_bf16x2(g0, g1);
             dd[2 * h + 1] = pack_bf16x2(g2, g3);
           }
