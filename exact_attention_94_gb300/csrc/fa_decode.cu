@@ -112,6 +112,21 @@ __global__ void __launch_bounds__(kDecThreads, 1) fa_decode_split_kernel(const D
     // ============================================================ producer
     if (lane == 0) {
       bool ok = true;
+      // paged: the key's logical block and slot, advanced key by key; the block
+      // table is read once per page, when the walk enters it
+      int pblk = 0, pslot = 0, page = 0;
+      auto lookup = [&]() {
+        page = p.block_table[(size_t)b * p.max_blocks + pblk];
+        if (page < 0 || page >= p.num_pages) {  // report, and read a valid page instead
+          atomicCAS(p.err, 0u, FA_DEVERR_BAD_PAGE);
+          page = 0;
+        }
+      };
+      if (p.block_table != nullptr && n_keys > 0) {
+        pblk = l0 / p.page_size;
+        pslot = l0 - pblk * p.page_size;
+        lookup();
+      }
       for (int s = 0; s < n_st && ok; ++s) {
         const int slot = s % NS;
         if (s >= NS && !(ok = mbar_wait(EMPTY(slot), ((s / NS) - 1) & 1, w, 41))) break;
@@ -122,12 +137,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) fa_decode_split_kernel(const D
           const int l = l0 + s * kDecT + m;
           size_t row;
           if (p.block_table != nullptr) {  // paged: logical block -> physical page
-            int page = p.block_table[(size_t)b * p.max_blocks + l / p.page_size];
-            if (page < 0 || page >= p.num_pages) {  // report, and read a valid page instead
-              atomicCAS(p.err, 0u, FA_DEVERR_BAD_PAGE);
-              page = 0;
+            row = ((size_t)page * p.page_size + pslot) * p.Hkv * D + kv_head0;
+            if (++pslot == p.page_size) {
+              pslot = 0;
+              ++pblk;
+              if (l + 1 < l1) lookup();  // the next key lies on the next page
             }
-            row = ((size_t)page * p.page_size + l % p.page_size) * p.Hkv * D + kv_head0;
           } else {
             row = ((size_t)b * p.L + l) * p.Hkv * D + kv_head0;
           }
