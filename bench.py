@@ -10,6 +10,7 @@ Q, K, V and dO are 67 MB each (268 MB together), larger than the 129 MB L2,
 so no L2 flush is needed between steps.
 
 Launch:  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+         python bench.py --case NAME [--batch B] [--iters K]   (one workload, for profilers)
 For N > 1 the driver starts one process per GPU with torchrun; every rank
 runs the same workload on its own GPU (independent replicas: the units of this
 path, (batch, head) pairs, need no exchange), and rank 0 prints one JSON line
@@ -52,7 +53,65 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads' sub-measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", choices=CASES, default=None,
+                    help="run one workload --iters times on cuda:0 and exit (for profilers; prints no bench line)")
+    ap.add_argument("--batch", type=int, default=0, help="--case: override the batch (dense, decode)")
+    ap.add_argument("--iters", type=int, default=3, help="--case: calls of the workload")
     return ap.parse_args()
+
+
+CASES = ["long", "mid", "varlen", "decode", "fp8", "window", "prefill"]
+
+
+def run_case(a):
+    """Runs one named workload a few times on cuda:0 for a profiler:
+    long / mid (fa_fwd + fa_bwd), varlen (packed fwd + bwd), decode (split-KV),
+    fp8 (quantise + e4m3 forward on the long shape), window (4096-key causal
+    window, fwd + bwd), prefill (chunked-prefill forward).  Inputs are the
+    seeded synthetic tensors of the benchmark workloads; the batch of the dense
+    and decode cases can be reduced so that a profiler's save and restore of
+    device memory stays small.  Returns the process exit status."""
+    import torch
+
+    import synth
+    from exact_attention_94_gb300 import ops
+
+    w = synth.WORKLOADS["long" if a.case == "fp8" else a.case]
+    B = a.batch or w.B
+    if a.case == "fp8":
+        x = synth.make_dense(B, w.H, w.N, w.d, seed=w.seed, k_boost=w.k_boost, device="cuda", with_do=False)
+        signs = synth.hadamard_signs(w.d, 0).cuda()
+        for _ in range(a.iters):
+            ops.fwd_fp8(x["q"], x["k"], x["v"], signs, causal=True)
+    elif a.case == "window":
+        x = synth.make_dense(B, w.H, w.N, w.d, seed=0, device="cuda")
+        for _ in range(a.iters):
+            o, lse = ops.fwd_masked(x["q"], x["k"], x["v"], window=w.window)
+            ops.bwd_masked(x["q"], x["k"], x["v"], o, lse, x["do"], window=w.window)
+    elif a.case == "prefill":
+        x = synth.make_masked(B, w.N, w.n_k, w.H, w.h_kv, w.d, seed=0, device="cuda", with_do=False)
+        for _ in range(a.iters):
+            ops.fwd_masked(x["q"], x["k"], x["v"], window=w.window)
+    elif a.case == "decode":
+        x = synth.make_decode(B, w.H, w.N, w.d, seed=0, device="cuda")
+        for _ in range(a.iters):
+            ops.decode(x["q"], x["k"], x["v"])
+    elif a.case == "varlen":
+        lengths = synth.varlen_lengths(w.B, w.len_lo, w.len_hi, w.seed)
+        x = synth.make_varlen(lengths, w.H, w.d, seed=0, device="cuda")
+        cu = x["cu_seqlens"].cuda()
+        for _ in range(a.iters):
+            o, lse = ops.fwd_varlen(x["q"], x["k"], x["v"], cu, int(lengths.max()), causal=True)
+            ops.bwd_varlen(x["q"], x["k"], x["v"], o, lse, x["do"], cu, int(lengths.max()), causal=True)
+    else:
+        x = synth.make_dense(B, w.H, w.N, w.d, seed=0, k_boost=w.k_boost, device="cuda")
+        for _ in range(a.iters):
+            o, lse = ops.fwd(x["q"], x["k"], x["v"], causal=w.causal)
+            ops.bwd(x["q"], x["k"], x["v"], o, lse, x["do"], causal=w.causal)
+    torch.cuda.synchronize()
+    err = ops.device_error()
+    print(f"{a.case}: {a.iters} iterations, device error {err}")
+    return 0 if err == 0 else 1
 
 
 def load_peaks():
@@ -260,6 +319,18 @@ def run_ours(args):
                        "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4), "traffic": traffic,
                        "peak_source": f"{peaks['source']} bf16 burst"}
     res["clocks"] = clocks.summary()
+    # The same rate against the tensor pipe's issue limit at the clock the bench
+    # actually ran at: 8192 bf16 FLOP per clock per SM (an M = N = 128, K = 16
+    # product issues every 64 cycles), times the SMs, times the sampled median
+    # SM clock.  The measured GEMM peak above was taken at whatever clock the
+    # GEMM loop held under the power cap, so the two fractions differ.
+    n_sm = torch.cuda.get_device_properties(local).multi_processor_count
+    mhz = res["clocks"].get("sm_mhz")
+    if mhz:
+        at_clock = 8192.0 * n_sm * mhz * 1e6 / 1e12
+        res["roofline"]["clock_normalised"] = {
+            "sm_mhz": mhz, "sms": n_sm, "flop_per_clk_per_sm": 8192, "peak_at_clock": round(at_clock, 1),
+            "frac": round(ach / at_clock, 4), "fwd_frac": round(fwd_tf / at_clock, 4)}
     res["gpu_launches"] = args.steps * (1 + (3 if have_bwd else 0))
     return res, (x, o, lse, ws, have_bwd, F)
 
@@ -532,6 +603,8 @@ def run_reference(args):
 
 def main():
     args = parse_args()
+    if args.case is not None:
+        sys.exit(run_case(args))
     rank, world, _ = dist_env()
     if args.impl == "reference":
         res = run_reference(args)

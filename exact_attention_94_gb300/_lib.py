@@ -54,6 +54,7 @@ SIGNATURES = {
     "fa_decode_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _F, _P]),
     "fa_device_error": (_I, [ctypes.POINTER(ctypes.c_uint)]),
     "fa_selftest_wait_timeout": (_I, [ctypes.c_double, _P]),
+    "fa_selftest_exp2": (_I, [_P, _P, _I, _I, _P]),
     "fa_set_option": (_I, [_I, ctypes.c_double]),
 }
 

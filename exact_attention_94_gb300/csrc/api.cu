@@ -34,21 +34,42 @@ __global__ void fa_wait_selftest_kernel(unsigned* err, unsigned long long timeou
   mbar_wait(smem_u32(&bar), 0, w, kSelftestSite);
 }
 
+// Evaluates one of the library's exp2 implementations elementwise (self-test);
+// each thread takes two neighbouring elements (the packed cubic works on pairs).
+__global__ void fa_exp2_selftest_kernel(const float* __restrict__ x, float* __restrict__ y, int n, int which) {
+  const long long i = 2ll * (blockIdx.x * (long long)blockDim.x + threadIdx.x);
+  if (i >= n) return;
+  const bool two = i + 1 < n;
+  const float v0 = x[i], v1 = two ? x[i + 1] : 0.f;
+  float y0, y1;
+  if (which == 0) {
+    y0 = ex2_poly(v0);
+    y1 = ex2_poly(v1);
+  } else if (which == 1) {
+    y0 = ex2_sfu(v0);
+    y1 = ex2_sfu(v1);
+  } else if (which == 2) {
+    y0 = exp2f(v0);
+    y1 = exp2f(v1);
+  } else {
+    ex2_poly2(v0, v1, y0, y1);
+  }
+  y[i] = y0;
+  if (two) y[i + 1] = y1;
+}
+
 namespace {
 
 struct Options {
   float tau = 8.0f;
-  bool poly = false;
+  int poly = 0;  // one column pair in `poly` on the cubic (0 = none)
   unsigned long long timeout_ns = 2000000000ull;
 } g_opt;
 
 std::once_flag g_init_once;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-constexpr int kMaxErrDevices = 64;
-std::mutex g_err_mutex;
-unsigned* g_err_ptrs[kMaxErrDevices] = {};   // device address of g_fa_error, per device ordinal
-thread_local unsigned* g_err_ptr = nullptr;  // the current device's, set by ensure_init()
+thread_local unsigned* g_err_ptr = nullptr;  // the current device's error word, set by ensure_init()
 
 void init_once() {
   cudaDriverEntryPointQueryResult q;
@@ -60,20 +81,16 @@ void init_once() {
 }
 
 // Every entry point calls this before it builds kernel parameters: it resolves
-// the driver entry point once per process and the error word's device address
-// once per device (the symbol has an address of its own on each device).
+// the driver entry point once per process, and looks up the error word's
+// device address on every call, with the caller's device current (the symbol
+// has an address of its own on each device, and a new one after the device's
+// context is torn down and created again; the lookup allocates nothing).
 bool ensure_init() {
   std::call_once(g_init_once, init_once);
   if (g_encode == nullptr) return false;
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxErrDevices) return false;
-  std::lock_guard<std::mutex> lock(g_err_mutex);
-  if (g_err_ptrs[dev] == nullptr) {
-    void* ep = nullptr;
-    if (cudaGetSymbolAddress(&ep, g_fa_error) != cudaSuccess || ep == nullptr) return false;
-    g_err_ptrs[dev] = static_cast<unsigned*>(ep);
-  }
-  g_err_ptr = g_err_ptrs[dev];
+  void* ep = nullptr;
+  if (cudaGetSymbolAddress(&ep, g_fa_error) != cudaSuccess || ep == nullptr) return false;
+  g_err_ptr = static_cast<unsigned*>(ep);
   return true;
 }
 
@@ -135,9 +152,16 @@ fa_status fa_set_option(fa_option opt, double value) {
       if (!(value >= 0.0 && value <= 64.0)) return FA_ERR_INVALID_ARG;
       g_opt.tau = (float)value;
       return FA_OK;
-    case FA_OPT_POLY_EXP:
-      g_opt.poly = value != 0.0;
-      return FA_OK;
+    case FA_OPT_POLY_EXP:  // 0 = off, 1 = the default share (1/8), or the share's denominator 4, 8, 16
+      if (value == 0.0 || value == 4.0 || value == 8.0 || value == 16.0) {
+        g_opt.poly = (int)value;
+        return FA_OK;
+      }
+      if (value == 1.0) {
+        g_opt.poly = 8;
+        return FA_OK;
+      }
+      return FA_ERR_INVALID_ARG;
     case FA_OPT_WAIT_TIMEOUT_MS:
       if (!(value >= 1.0 && value <= 600000.0)) return FA_ERR_INVALID_ARG;
       g_opt.timeout_ns = (unsigned long long)(value * 1e6);
@@ -150,6 +174,15 @@ fa_status fa_selftest_wait_timeout(double timeout_ms, fa_stream_t stream) {
   if (!(timeout_ms >= 1.0 && timeout_ms <= 10000.0)) return FA_ERR_INVALID_ARG;
   if (!ensure_init()) return FA_ERR_LAUNCH;
   fa_wait_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(g_err_ptr, (unsigned long long)(timeout_ms * 1e6));
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+fa_status fa_selftest_exp2(const float* x, float* y, int n, int which, fa_stream_t stream) {
+  if (n < 0 || which < 0 || which > 3 || (n > 0 && (!x || !y))) return FA_ERR_INVALID_ARG;
+  if (((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 3u) != 0) return FA_ERR_MISALIGNED;
+  if (n == 0) return FA_OK;
+  const long long pairs = ((long long)n + 1) / 2;
+  fa_exp2_selftest_kernel<<<(unsigned)((pairs + 255) / 256), 256, 0, (cudaStream_t)stream>>>(x, y, n, which);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
@@ -210,11 +243,15 @@ static fa_status fwd_common(const void* q, const void* k, const void* v, void* o
   p.win_left = wl;
   p.win_right = wr;
   p.num_pairs = num_pairs;
+  p.max_len = max_len;
+  p.max_len_k = max_len_k;
   p.scale_log2 = scale * kLog2e;
   p.tau = g_opt.tau;
   p.err = g_err_ptr;
   p.timeout_ns = g_opt.timeout_ns;
-  cudaError_t e = launch_fwd(tq, tk, tv, p, d, mask_kind(wl, wr), g_opt.poly, nbatch * H, (cudaStream_t)stream);
+  const int mk = mask_kind(wl, wr);
+  const int poly = (mk == kMaskWindow && g_opt.poly != 0) ? 8 : g_opt.poly;
+  cudaError_t e = launch_fwd(tq, tk, tv, p, d, mk, poly, nbatch * H, (cudaStream_t)stream);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
@@ -342,6 +379,8 @@ static fa_status bwd_common(const void* q, const void* k, const void* v, const v
   p.win_left = wl;
   p.win_right = wr;
   p.num_kblocks = num_kblocks;
+  p.max_len = max_len;
+  p.max_len_k = max_len_k;
   p.scale = scale;
   p.scale_log2 = scale * kLog2e;
   p.err = g_err_ptr;
@@ -412,12 +451,6 @@ fa_status fa_bwd_masked_varlen(const void* q, const void* k, const void* v, cons
 // holds these bytes until the process exits.  All calls share it.
 static __device__ __align__(256) unsigned char g_bwd_scratch[FA_BWD_NOALLOC_SCRATCH_BYTES];
 
-namespace {
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};  // device address of g_bwd_scratch, per device ordinal
-}  // namespace
-
 fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
                          const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
                          float scale, fa_stream_t stream) {
@@ -425,20 +458,12 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
   if (N == 0) return FA_OK;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if (fa_bwd_workspace_bytes(B, H, N, d) > (size_t)FA_BWD_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_LIMIT;
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_LAUNCH;
+  // The array's device address, looked up with the caller's device current on
+  // every call (in host code the symbol itself is only a stand-in; the lookup
+  // allocates nothing, and a context created anew after a device reset gets a
+  // new address).
   void* scratch = nullptr;
-  {
-    // First call on this device: look up the array's device address with the
-    // device current (in host code the symbol itself is only a stand-in).
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
-      void* ptr = nullptr;
-      if (cudaGetSymbolAddress(&ptr, g_bwd_scratch) != cudaSuccess || ptr == nullptr) return FA_ERR_LAUNCH;
-      g_scratch_ptr[dev] = ptr;
-    }
-    scratch = g_scratch_ptr[dev];
-  }
+  if (cudaGetSymbolAddress(&scratch, g_bwd_scratch) != cudaSuccess || scratch == nullptr) return FA_ERR_LAUNCH;
   // The pre-kernel of the backward zeroes the accumulator part of the scratch
   // and overwrites the per-row arrays, so the previous call's contents never leak.
   return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, scratch, nullptr, nullptr, B, N, N, N, N, N, N, H, H, d, -1,
@@ -508,6 +533,8 @@ fa_status fa_fwd_fp8(const void* q_codes, const void* k_codes, const void* vt_co
   p.win_left = wl;
   p.win_right = wr;
   p.num_pairs = num_pairs;
+  p.max_len = Nq;
+  p.max_len_k = Nk;
   p.q_scale = q_scale;
   p.k_scale = k_scale;
   p.v_scale = v_scale;
@@ -517,7 +544,8 @@ fa_status fa_fwd_fp8(const void* q_codes, const void* k_codes, const void* vt_co
   p.tau = g_opt.tau;
   p.err = g_err_ptr;
   p.timeout_ns = g_opt.timeout_ns;
-  cudaError_t e = launch_fwd_fp8(tq, tk, tvt, p, mask_kind(wl, wr), g_opt.poly, B * Hq, (cudaStream_t)stream);
+  cudaError_t e = launch_fwd_fp8(tq, tk, tvt, p, mask_kind(wl, wr), g_opt.poly != 0 ? 8 : 0, B * Hq,
+                                 (cudaStream_t)stream);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

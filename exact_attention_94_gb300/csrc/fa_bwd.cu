@@ -175,7 +175,7 @@ struct BwdItem {
   int b_coord;             // batch coordinate of the tensors (0 when packed)
   int off;                 // kv_len - seq_len
   int q_lo, q_hi;
-  bool bad;                // packed offsets outside the tensors
+  bool bad;                // packed offsets outside the tensors, or longer than the stated maxima
 };
 
 template <int MASK>
@@ -188,7 +188,8 @@ __device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int b, int k0) {
     it.kv_len = p.cu_seqlens_k[b + 1] - it.kv_start;
     it.b_coord = 0;
     it.bad = it.seq_start < 0 || it.seq_len < 0 || it.seq_start > p.n_rows - it.seq_len || it.kv_start < 0 ||
-             it.kv_len < 0 || it.kv_start > p.n_rows_k - it.kv_len;
+             it.kv_len < 0 || it.kv_start > p.n_rows_k - it.kv_len || it.seq_len > p.max_len ||
+             it.kv_len > p.max_len_k;  // a sequence longer than the stated maximum would lose rows
   }
   it.off = it.kv_len - it.seq_len;
   it.q_lo = 0;
@@ -761,14 +762,9 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
 
   auto kern = main_kernel_for<D, MASK>();
   constexpr uint32_t smem = Bwd128Layout<D>::kBytes;
-  static bool configured[64] = {};  // the shared-memory limit is a per-device function attribute
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
+  // set on every launch: the attribute belongs to the current device's context
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
   const int bh = p.B * (p.H / p.kv_group);  // CTAs walk (batch, K/V head) pairs
   const int gx = bh < kBwdHeadGroup ? bh : kBwdHeadGroup;
   dim3 grid(gx, p.num_kblocks, (bh + gx - 1) / gx);

@@ -21,7 +21,8 @@
 // natively; tiles outside every row's window are never visited, the
 // block-sparse skipping that FlexAttention's block mask performs).
 // Part of the exponentials may be evaluated on the FMA pipe as
-// 2^floor(x) * p3(x - floor(x)) with a cubic fitted in fit_exp2_poly.py.
+// 2^floor(x) * p3(x - floor(x)) with a cubic fitted in fit_exp2_poly.py: one
+// column pair in POLYK (template argument; 0 = none) goes to the cubic.
 //
 // CTA organisation (one CTA per pair of 128-row query tiles of one head):
 //   warp 0      TMA producer: Q tiles once, then K_j, V_j into a ring of slots
@@ -57,7 +58,7 @@ constexpr int kHeadGroup = 8;  // heads whose CTAs are scheduled together
 
 }  // namespace
 
-template <int D, int MASK, bool POLY, bool F8>
+template <int D, int MASK, int POLYK, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -95,7 +96,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     kv_len = p.cu_seqlens_k[b + 1] - kv_start;
     b_coord = 0;
     if (seq_start < 0 || seq_len < 0 || seq_start > p.n_rows - seq_len || kv_start < 0 || kv_len < 0 ||
-        kv_start > p.n_rows_k - kv_len) {  // offsets outside the tensors: report, touch nothing
+        kv_start > p.n_rows_k - kv_len || seq_len > p.max_len || kv_len > p.max_len_k) {
+      // offsets outside the tensors, or a sequence longer than the stated maximum: report, touch nothing
       if (threadIdx.x == 0 && p.err != nullptr) atomicCAS(p.err, 0u, FA_DEVERR_BAD_SEQLEN);
       return;
     }
@@ -399,9 +401,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float y0, y1;
         f2_unpack(f2_fma(f2_pack(x[2 * i], x[2 * i + 1]), sl2x2, nmb2), y0, y1);
         float p0, p1;
-        if (POLY && (i & 7) == 7) {
-          p0 = ex2_poly(y0);
-          p1 = ex2_poly(y1);
+        if (POLYK > 0 && (i % POLYK) == POLYK - 1) {
+          ex2_poly2(y0, y1, p0, p1);
         } else {
           p0 = ex2_sfu(y0);
           p1 = ex2_sfu(y1);
@@ -492,19 +493,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, int MASK, bool POLY, bool F8>
+template <int D, int MASK, int POLYK, bool F8>
 static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const FwdParams& p, int grid_x, cudaStream_t stream) {
-  auto kern = fa_fwd_kernel<D, MASK, POLY, F8>;
+  auto kern = fa_fwd_kernel<D, MASK, POLYK, F8>;
   constexpr uint32_t smem = FwdLayout<D, F8>::kBytes;
-  static bool configured[64] = {};  // the shared-memory limit is a per-device function attribute
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
+  // The shared-memory limit is a function attribute of the current device's
+  // context; it is set on every launch (no cached per-device state to go stale
+  // or to race on between host threads).
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
   const int gx = grid_x < kHeadGroup ? grid_x : kHeadGroup;
   dim3 grid(gx, p.num_pairs, (grid_x + gx - 1) / gx);
   kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
@@ -512,16 +510,22 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
 }
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
-                       int D, int mask, bool poly, int grid_x, cudaStream_t stream) {
+                       int D, int mask, int poly, int grid_x, cudaStream_t stream) {
 #define FA_FWD_CASE(DD, MM, PP) \
   if (D == DD && mask == MM && poly == PP) return launch_fwd_t<DD, MM, PP, false>(tq, tk, tv, p, grid_x, stream);
-#define FA_FWD_CASES(DD)         \
-  FA_FWD_CASE(DD, kMaskNone, false)   \
-  FA_FWD_CASE(DD, kMaskNone, true)    \
-  FA_FWD_CASE(DD, kMaskRight, false)  \
-  FA_FWD_CASE(DD, kMaskRight, true)   \
-  FA_FWD_CASE(DD, kMaskWindow, false) \
-  FA_FWD_CASE(DD, kMaskWindow, true)
+  // the cubic's share is selectable (1/4, 1/8, 1/16 of the column pairs) for
+  // the unmasked and causal kernels; the windowed ones take 1/8 or none
+#define FA_FWD_CASES(DD)            \
+  FA_FWD_CASE(DD, kMaskNone, 0)     \
+  FA_FWD_CASE(DD, kMaskNone, 4)     \
+  FA_FWD_CASE(DD, kMaskNone, 8)     \
+  FA_FWD_CASE(DD, kMaskNone, 16)    \
+  FA_FWD_CASE(DD, kMaskRight, 0)    \
+  FA_FWD_CASE(DD, kMaskRight, 4)    \
+  FA_FWD_CASE(DD, kMaskRight, 8)    \
+  FA_FWD_CASE(DD, kMaskRight, 16)   \
+  FA_FWD_CASE(DD, kMaskWindow, 0)   \
+  FA_FWD_CASE(DD, kMaskWindow, 8)
   FA_FWD_CASES(64)
   FA_FWD_CASES(128)
 #undef FA_FWD_CASES
@@ -530,15 +534,15 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
 }
 
 cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt, const FwdParams& p,
-                           int mask, bool poly, int grid_x, cudaStream_t stream) {
+                           int mask, int poly, int grid_x, cudaStream_t stream) {
 #define FA_FP8_CASE(MM, PP) \
   if (mask == MM && poly == PP) return launch_fwd_t<128, MM, PP, true>(tq, tk, tvt, p, grid_x, stream);
-  FA_FP8_CASE(kMaskNone, false)
-  FA_FP8_CASE(kMaskNone, true)
-  FA_FP8_CASE(kMaskRight, false)
-  FA_FP8_CASE(kMaskRight, true)
-  FA_FP8_CASE(kMaskWindow, false)
-  FA_FP8_CASE(kMaskWindow, true)
+  FA_FP8_CASE(kMaskNone, 0)
+  FA_FP8_CASE(kMaskNone, 8)
+  FA_FP8_CASE(kMaskRight, 0)
+  FA_FP8_CASE(kMaskRight, 8)
+  FA_FP8_CASE(kMaskWindow, 0)
+  FA_FP8_CASE(kMaskWindow, 8)
 #undef FA_FP8_CASE
   return cudaErrorInvalidValue;
 }

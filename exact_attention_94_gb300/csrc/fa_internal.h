@@ -24,6 +24,8 @@ struct FwdParams {
   int win_left;              // mask (used by the masked kernels): query i sees keys
   int win_right;             //   [i + Nk - Nq - win_left, i + Nk - Nq + win_right]; -1 = unbounded side
   int num_pairs;             // grid.y: pairs of 128-row query tiles per (sequence, head)
+  int max_len;               // longest query sequence the caller declared (packed: max_seqlen_q)
+  int max_len_k;             // longest key sequence the caller declared
   // e4m3 operands only: one scale per 128-row block, [B][H][n_qblk] for Q and
   // [B][Hkv][n_kblk] for K and V (V's codes are stored transposed per head)
   const float* q_scale;
@@ -60,6 +62,8 @@ struct BwdParams {
   int win_left;              // mask, as in FwdParams
   int win_right;
   int num_kblocks;           // grid.y of the main kernel
+  int max_len;               // longest query / key sequence the caller declared (packed calls)
+  int max_len_k;
   float scale;
   float scale_log2;
   unsigned* err;
@@ -77,13 +81,15 @@ inline int mask_kind(int win_left, int win_right) {
   return win_left >= 0 ? kMaskWindow : (win_right >= 0 ? kMaskRight : kMaskNone);
 }
 
+// poly: one column pair in `poly` of the softmax exponentials on the FMA-pipe
+// cubic (0 = all on the SFU; 4, 8 or 16; masks with a left bound: 0 or 8).
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
-                       int D, int mask, bool poly, int grid_x, cudaStream_t stream);
+                       int D, int mask, int poly, int grid_x, cudaStream_t stream);
 
 // Forward on e4m3 operands (d = 128): tq, tk over codes [B][N][H][d] (uint8),
 // tv over V's codes transposed [B][Hkv][d][n_pad].
 cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt, const FwdParams& p,
-                           int mask, bool poly, int grid_x, cudaStream_t stream);
+                           int mask, int poly, int grid_x, cudaStream_t stream);
 
 // Block quantisation to e4m3 (d = 64 or 128): x [B][N][H][d] bf16 -> codes and
 // one fp32 scale per 128-row block [B][H][ceil(N/128)].  rotate: multiply each

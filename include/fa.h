@@ -130,8 +130,10 @@ fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
  *   lse        : [H, total_tokens] fp32, written
  *   cu_seqlens : int32 [num_seqs + 1], DEVICE memory, non-decreasing,
  *                cu_seqlens[0] = 0, cu_seqlens[num_seqs] = total_tokens
- *   max_seqlen : an upper bound of every sequence length (sizes the grid;
- *                rows of a longer sequence beyond it are not computed)
+ *   max_seqlen : an upper bound of every sequence length.  A sequence longer
+ *                than it, or offsets outside the tensors, are reported by
+ *                fa_device_error (FA_ERR_INVALID_ARG, code 0x2001) and nothing
+ *                is written for that sequence
  */
 fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens,
                         int num_seqs, int max_seqlen, int total_tokens, int H, int d, int causal, float scale,
@@ -140,7 +142,9 @@ fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, fl
 /* Scratch bytes fa_bwd_varlen needs (same two buffers over total_tokens rows). */
 size_t fa_bwd_varlen_workspace_bytes(int total_tokens, int H, int d);
 
-/* Backward pass of fa_fwd_varlen; tensors as in fa_bwd in the packed layout. */
+/* Backward pass of fa_fwd_varlen; tensors as in fa_bwd in the packed layout.
+ * Sequences longer than max_seqlen or outside the tensors are reported as in
+ * fa_fwd_varlen, and their dK, dV rows are not written. */
 fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
                         const void* dout, void* dq, void* dk, void* dv, void* workspace, const int* cu_seqlens,
                         int num_seqs, int max_seqlen, int total_tokens, int H, int d, int causal, float scale,
@@ -180,7 +184,8 @@ fa_status fa_fwd_masked(const void* q, const void* k, const void* v, void* o, fl
  *                fa_fwd_varlen; offsets outside the tensors are reported by
  *                fa_device_error (FA_ERR_INVALID_ARG) and nothing is written
  *                for that sequence
- *   max_seqlen_q, max_seqlen_k : upper bounds of the sequences' lengths
+ *   max_seqlen_q, max_seqlen_k : upper bounds of the sequences' lengths (a
+ *                longer sequence is reported like a bad offset)
  */
 fa_status fa_fwd_masked_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
                                const int* cu_seqlens_q, const int* cu_seqlens_k, int num_seqs, int max_seqlen_q,
@@ -324,9 +329,12 @@ fa_status fa_paged_append(const void* k_new, const void* v_new, void* k_pages, v
  *   Limit: fa_bwd_workspace_bytes(B, H, N, d) <= FA_BWD_NOALLOC_SCRATCH_BYTES
  *          (for d = 128 about 64 K rows of B*H*N, for d = 64 about 125 K);
  *          larger problems return FA_ERR_SCRATCH_LIMIT without launching.
- *   Set-up: the first call on each device looks up the scratch array's device
- *          address with that device current; make that first call before
- *          any stream capture.
+ *   Set-up: every call looks up the scratch array's device address with the
+ *          caller's device current (cudaGetSymbolAddress, which allocates
+ *          nothing), so a context created anew after cudaDeviceReset gets the
+ *          new address.  On a device's first call the lookup also makes the
+ *          runtime load the library's kernels there: make that first call
+ *          before any stream capture.
  *   Sharing: every call on a device uses the same scratch.  The kernels clear
  *          what must start at zero, but two calls whose work overlaps on the
  *          GPU (different streams, or host threads racing) corrupt each
@@ -441,12 +449,35 @@ fa_status fa_device_error(unsigned int* code);
 fa_status fa_selftest_wait_timeout(double timeout_ms, fa_stream_t stream);
 
 /*
+ * Self-test of the exponentials the forward kernel can use ("efficient-
+ * attention/flash-2-3", section "And on Blackwell": part of the exponentials
+ * are computed on the FMA units as 2^x = 2^floor(x) * p3(x - floor(x)) with a
+ * cubic p3, instead of on the special-function unit).  Evaluates, for each of
+ * the n fp32 values x[i] (device), y[i] = (device, written)
+ *   which = 0 : the kernel's cubic (inputs below -127 are clamped to -127;
+ *               coefficients fitted in fit_exp2_poly.py, relative error
+ *               8.6e-5 on [-126, 0])
+ *   which = 1 : the special-function unit's ex2.approx.ftz.f32
+ *   which = 2 : CUDA's exp2f
+ *   which = 3 : the cubic evaluated two values at a time with the packed
+ *               f32x2 instructions (the form the forward kernel uses); bit
+ *               for bit equal to which = 0
+ * x and y 4-byte aligned.  The pages print no error bound; the test compares
+ * the cubic with float64 2^x and with exp2f.
+ */
+fa_status fa_selftest_exp2(const float* x, float* y, int n, int which, fa_stream_t stream);
+
+/*
  * Developer knobs (process-wide; they change speed, not results beyond
  * rounding):
  *   FA_OPT_RESCALE_TAU   : lazy-rescale threshold in log2 units (default 8;
  *                          0 rescales whenever the running maximum grows)
- *   FA_OPT_POLY_EXP      : 1 = evaluate a share of the exponentials with the
- *                          cubic on the FMA pipe, 0 = all on the SFU
+ *   FA_OPT_POLY_EXP      : share of the forward's softmax exponentials
+ *                          evaluated with the cubic on the FMA pipe: 0 = none
+ *                          (all on the SFU), 4 / 8 / 16 = one column pair in
+ *                          4 / 8 / 16, 1 = 8 (sliding-window and FP8 kernels:
+ *                          any nonzero value means 8); other values give
+ *                          FA_ERR_INVALID_ARG
  *   FA_OPT_WAIT_TIMEOUT_MS : limit of every bounded wait (default 2000)
  */
 typedef enum { FA_OPT_RESCALE_TAU = 1, FA_OPT_POLY_EXP = 2, FA_OPT_WAIT_TIMEOUT_MS = 3 } fa_option;

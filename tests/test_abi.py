@@ -82,6 +82,11 @@ def test_options(lib):
     assert lib.fa_set_option(_lib.FA_OPT_RESCALE_TAU, 8.0) == _lib.FA_OK
     assert lib.fa_set_option(99, 1.0) == _lib.FA_ERR_INVALID_ARG
     assert lib.fa_set_option(_lib.FA_OPT_WAIT_TIMEOUT_MS, 0.0) == _lib.FA_ERR_INVALID_ARG
+    for share in (0.0, 1.0, 4.0, 8.0, 16.0):  # the cubic's share: none, default, one pair in 4 / 8 / 16
+        assert lib.fa_set_option(_lib.FA_OPT_POLY_EXP, share) == _lib.FA_OK
+    for share in (2.0, 3.0, -1.0, 32.0):
+        assert lib.fa_set_option(_lib.FA_OPT_POLY_EXP, share) == _lib.FA_ERR_INVALID_ARG
+    assert lib.fa_set_option(_lib.FA_OPT_POLY_EXP, 0.0) == _lib.FA_OK
 
 
 def test_masked_validation(lib):

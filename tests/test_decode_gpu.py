@@ -9,8 +9,8 @@ import torch
 
 import oracle
 import synth
-from exact_attention_94_gb300 import ops
-from tests.parity import assert_lse, assert_o
+from exact_attention_94_gb300 import _lib, ops
+from tests.parity import LSE_TOL, O_TOL, assert_lse, assert_o
 
 pytestmark = pytest.mark.gpu
 
@@ -28,9 +28,13 @@ def run_decode(B, H, L, d, num_splits, seed=0):
 @pytest.mark.parametrize("L", [1, 3, 4, 5, 127, 1000])
 @pytest.mark.parametrize("num_splits", [0, 1, 2, 7])
 def test_decode_small(d, L, num_splits):
-    if num_splits > L:
-        pytest.skip("more splits than keys")
     B, H = 3, 4
+    if num_splits > L:  # more splits than keys: refused before any launch
+        x = synth.make_decode(B, H, L, d, seed=L)
+        with pytest.raises(_lib.FaError) as e:
+            ops.decode(*(x[n].cuda() for n in ("q", "k", "v")), num_splits=num_splits)
+        assert e.value.status == _lib.FA_ERR_INVALID_ARG
+        return
     x, o, lse = run_decode(B, H, L, d, num_splits, seed=L)
     o_ref, l_ref = oracle.decode_forward(*(synth.to_f64(x[n]) for n in ("q", "k", "v")), 1.0 / math.sqrt(d))
     assert_o(synth.to_f64(o), o_ref, f"decode O L{L} d{d} S{num_splits}")
@@ -156,8 +160,11 @@ def test_decode_window(d, wl, num_splits):
     kc = torch.randn((B, L, Hkv, d), generator=g).to(torch.bfloat16)
     vc = torch.randn((B, L, Hkv, d), generator=g).to(torch.bfloat16)
     span = L if wl < 0 or wl >= L else wl + 1
-    if num_splits > span:
-        pytest.skip("more splits than keys in the window")
+    if num_splits > span:  # more splits than keys in the window: refused before any launch
+        with pytest.raises(_lib.FaError) as e:
+            ops.decode_window(q.cuda(), kc.cuda(), vc.cuda(), wl, num_splits=num_splits)
+        assert e.value.status == _lib.FA_ERR_INVALID_ARG
+        return
     o, lse = ops.decode_window(q.cuda(), kc.cuda(), vc.cuda(), wl, num_splits=num_splits)
     torch.cuda.synchronize()
     assert ops.device_error() == 0
@@ -186,3 +193,77 @@ def test_paged_decode_window_grouped(wl):
         o_ref, l_ref = oracle.masked_forward(synth.to_f64(q[b:b + 1]), kb, vb, 1 / math.sqrt(d), wl, 0)
         assert_o(synth.to_f64(o[b:b + 1]), o_ref, f"paged window b{b}")
         assert_lse(lse[b:b + 1].cpu().numpy(), l_ref[:, :, 0], f"paged window b{b}")
+
+
+# ---------------------------------------------------------------- decode against the dense path
+#
+# "Decoding needs a different split" (efficient-attention/flash-2-3): the
+# split-KV decode computes the same single-query attention as the dense path,
+# only partitioned along the keys and merged.  Each case below runs the dense
+# masked forward with one query (N_q = 1, bottom-right aligned, so the query
+# sits at the last key) on the same cache and compares the two results within
+# the parity tolerances.
+
+def _dense_one_query(q, k, v, window_left=-1):
+    """fa_fwd_masked with N_q = 1 over a contiguous cache [B, L, Hkv, d]."""
+    o, lse = ops.fwd_masked(q, k, v, window=(window_left, -1))
+    return o, lse[:, :, 0]
+
+
+def _close(o_dec, l_dec, o_den, l_den, what):
+    do = (o_dec.double() - o_den.double()).abs().max().item()
+    dl = (l_dec - l_den).abs().max().item()
+    assert do <= O_TOL, f"{what}: max |O_decode - O_dense| {do:.3e}"
+    assert dl <= LSE_TOL, f"{what}: max |lse_decode - lse_dense| {dl:.3e}"
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("L,num_splits", [(1, 1), (129, 0), (1000, 3), (4096, 0), (4097, 7)])
+def test_decode_equals_dense_path(d, L, num_splits):
+    B, H = 3, 8
+    x = synth.make_decode(B, H, L, d, seed=L + d)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    o1, l1 = ops.decode(q, k, v, num_splits=num_splits)
+    o2, l2 = _dense_one_query(q, k, v)
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    _close(o1, l1, o2, l2, f"decode L{L} d{d} S{num_splits}")
+
+
+@pytest.mark.parametrize("Hq,Hkv,wl", [(32, 8, -1), (16, 1, -1), (12, 4, 300), (8, 2, 0)])
+def test_decode_gqa_window_equals_dense_path(Hq, Hkv, wl):
+    B, L, d = 2, 2000, 128
+    g = torch.Generator().manual_seed(Hq * 10 + Hkv + wl)
+    q = torch.randn((B, 1, Hq, d), generator=g).to(torch.bfloat16).cuda()
+    kc = torch.randn((B, L, Hkv, d), generator=g).to(torch.bfloat16).cuda()
+    vc = torch.randn((B, L, Hkv, d), generator=g).to(torch.bfloat16).cuda()
+    if wl < 0:
+        o1, l1 = ops.decode_gqa(q, kc, vc)
+    else:
+        o1, l1 = ops.decode_window(q, kc, vc, wl)
+    o2, l2 = _dense_one_query(q, kc, vc, wl)
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    _close(o1, l1, o2, l2, f"decode Hq{Hq} Hkv{Hkv} wl{wl}")
+
+
+@pytest.mark.parametrize("Hq,Hkv,wl", [(4, 4, -1), (8, 2, -1), (8, 2, 40)])
+def test_paged_decode_equals_dense_path(Hq, Hkv, wl):
+    """Each sequence's pages gathered into a contiguous cache on the device
+    (plain indexing), then the dense one-query forward on it."""
+    lengths = [1, 15, 16, 17, 100, 1000]
+    d, P = 128, 16
+    x = synth.make_paged_decode(lengths, Hkv, d, page_size=P, seed=Hq + Hkv + wl)
+    g = torch.Generator().manual_seed(Hq + 3 * Hkv + wl)
+    q = torch.randn((len(lengths), 1, Hq, d), generator=g).to(torch.bfloat16).cuda()
+    dev = {n: x[n].cuda() for n in x}
+    o1, l1 = ops.decode_paged_window(q, dev["k_pages"], dev["v_pages"], dev["block_table"], dev["seq_lens"],
+                                     max(lengths), wl, num_splits=3)
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    for b, Lb in enumerate(lengths):
+        pages = dev["block_table"][b, : (Lb + P - 1) // P].long()
+        kb = dev["k_pages"][pages].reshape(-1, Hkv, d)[:Lb][None].contiguous()
+        vb = dev["v_pages"][pages].reshape(-1, Hkv, d)[:Lb][None].contiguous()
+        o2, l2 = _dense_one_query(q[b:b + 1], kb, vb, wl)
+        _close(o1[b:b + 1], l1[b:b + 1], o2, l2, f"paged b{b} L{Lb} wl{wl}")

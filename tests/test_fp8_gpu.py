@@ -54,6 +54,23 @@ def test_quantizer_bit_exact(d, rotate, transpose):
     assert np.array_equal(c, ref_c), int(np.sum(c != ref_c))
 
 
+@pytest.mark.parametrize("rotate", [False, True])
+def test_quantizer_codes_within_one_step_of_the_quotient(rotate):
+    """The GPU codes against e4m3(x / scale) with the plain float32 quotient:
+    at most one code step apart, on a small fraction of elements (exact ties
+    of the quotient; see the oracle-side test of the same property)."""
+    from tests.test_oracle_fp8 import code_steps, quotient_codes
+    B, N, H, d = 2, 1024, 2, 128
+    x = synth.outlier_bf16((B, N, H, d), seed=31 + rotate, idx=0)
+    signs = _signs(d, seed=4) if rotate else None
+    codes, _ = ops.fp8_quantize(x.cuda(), signs.cuda() if rotate else None)
+    torch.cuda.synchronize()
+    plain, _ = quotient_codes(x.float().numpy(), signs.numpy().astype(np.float32) if rotate else None)
+    steps = code_steps(codes.cpu().numpy(), plain)
+    assert steps.max() <= 1
+    assert float(np.mean(steps > 0)) <= (2e-3 if not rotate else 1e-4)
+
+
 # ------------------------------------------------------------------ attention
 
 def _reference(x, signs, wl, wr, scale):

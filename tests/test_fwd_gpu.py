@@ -62,12 +62,17 @@ def test_several_tiles_with_max_jumps(d, causal):
 
 
 @pytest.mark.parametrize("tau", [0.0, 8.0, 30.0])
-@pytest.mark.parametrize("poly", [0, 1])
-def test_rescale_threshold_and_exp_split(tau, poly):
+@pytest.mark.parametrize("poly", [0, 4, 8, 16])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_rescale_threshold_and_exp_split(tau, poly, d, causal):
+    """Every lazy-rescale threshold and every share of exponentials on the
+    FMA-pipe cubic (0 = none, else one column pair in `poly`) gives the same
+    result within tolerance, at both head dims, with and without the mask."""
     ops.set_option(_lib.FA_OPT_RESCALE_TAU, tau)
     ops.set_option(_lib.FA_OPT_POLY_EXP, poly)
     try:
-        check_dense(1, 4, 1024, 128, True, seed=3, k_boost=3.0)
+        check_dense(1, 4, 1024 + 33, d, causal, seed=3, k_boost=3.0)
     finally:
         ops.set_option(_lib.FA_OPT_RESCALE_TAU, 8.0)
         ops.set_option(_lib.FA_OPT_POLY_EXP, 0)

@@ -278,3 +278,63 @@ def test_fp8_forward_close_to_exact_without_outliers():
     o8, l8 = F.fp8_forward(q, k, v, 128 ** -0.5, True, signs)
     o, l = A.forward(q.astype(np.float64), k.astype(np.float64), v.astype(np.float64), 128 ** -0.5, True)
     assert np.sqrt(np.mean((o8 - o) ** 2)) < 2e-2 and np.max(np.abs(l8 - l)) < 0.1
+
+
+# ------------------------------------------------------------------ reciprocal scale vs the plain quotient
+
+def quotient_codes(x32, signs=None, block_rows=128):
+    """e4m3(x / scale) with the quotient rounded once to float32: the plain
+    form of "divide by the block's scale" that the page's description implies
+    before any choice of how a kernel evaluates it."""
+    codes, scales = F.fp8_quantize(x32, signs, block_rows)
+    B, N, H, d = x32.shape
+    out = np.zeros_like(codes)
+    for b in range(B):
+        for h in range(H):
+            rows = np.asarray(x32[b, :, h], np.float32)
+            if signs is not None:
+                rows = F.rotate_f32(rows, signs)
+            for t, sc in enumerate(scales[b, h]):
+                if sc == 0:
+                    continue
+                blk = rows[t * block_rows:(t + 1) * block_rows]
+                out[b, t * block_rows:(t + 1) * block_rows, h] = F.e4m3_encode((blk / sc).astype(np.float32))
+    return out, codes
+
+
+def code_steps(a, b):
+    """Distance between two e4m3 codes along the number line (codes of one
+    sign are ordered by their low 7 bits); signs must agree unless both are 0."""
+    a = a.astype(np.int64)
+    b = b.astype(np.int64)
+    va = np.where(a & 0x80, -(a & 0x7F), a & 0x7F)
+    vb = np.where(b & 0x80, -(b & 0x7F), b & 0x7F)
+    return np.abs(va - vb)
+
+
+@pytest.mark.parametrize("rotate", [False, True])
+def test_reciprocal_codes_within_one_step_of_the_quotient(rotate):
+    """The quantiser multiplies by the float32 reciprocal of the scale
+    (reading in the oracle's header).  Against the plain quotient x / scale
+    the two float32 values differ by at most a couple of float32 ulps, so a
+    code can move only where an e4m3 rounding midpoint lies between them: at
+    most one code step, and only where the quotient sits on (or within a few
+    float32 ulps of) a midpoint.  Unrotated bf16 inputs hit exact ties when
+    the block maximum makes the scale a short binary fraction (24.5 / 448 =
+    0.0546875, say): measured 7e-4 of elements here; the rotated (float32
+    transform) inputs almost never do."""
+    x = np.asarray(_outlier_inputs(11, B=2, N=2048, H=2, d=128)[0], np.float32)
+    signs = np.where(np.random.default_rng(5).random(128) < 0.5, -1.0, 1.0).astype(np.float32) if rotate else None
+    plain, recip = quotient_codes(x, signs)
+    steps = code_steps(plain, recip)
+    assert steps.max() <= 1
+    frac = float(np.mean(steps > 0))
+    assert frac <= (2e-3 if not rotate else 1e-4), frac
+    # every differing element: the plain quotient lies within 4 float32 ulps of
+    # the midpoint between the two codes' values
+    codes, scales = F.fp8_quantize(x, signs)
+    for b, n, h, c in np.argwhere(steps > 0):
+        row = x[b, :, h] if signs is None else F.rotate_f32(x[b, :, h], signs)
+        y = np.float32(row[n, c] / scales[b, h, n // 128])
+        mid = 0.5 * (F.e4m3_decode(plain[b, n, h, c]) + F.e4m3_decode(recip[b, n, h, c]))
+        assert abs(float(y) - mid) <= 4 * float(np.spacing(np.abs(y))), (float(y), mid)

@@ -67,3 +67,24 @@ def test_varlen_workload_sampled_sequences():
             oh, lh = oracle.head_forward(qh, kh, vh, w.scale, True)
             assert_o(synth.to_f64(o[lo:hi, h]), oh, f"varlen seq{b} h{h}")
             assert_lse(lse[h, lo:hi].cpu().numpy(), lh, f"varlen seq{b} h{h}")
+
+
+@pytest.mark.parametrize("which", ["fwd", "bwd"])
+def test_max_seqlen_too_small_is_reported(which):
+    """A sequence longer than the declared max_seqlen would leave rows of it
+    uncomputed: the kernels report it (code 0x2001, FA_ERR_INVALID_ARG) and
+    write nothing for that sequence instead."""
+    lengths = [100, 600, 50]
+    x = synth.make_varlen(lengths, 2, 128, seed=6)
+    cu = x["cu_seqlens"].cuda()
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = ops.fwd_varlen(q, k, v, cu, max(lengths), causal=True)
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    if which == "fwd":
+        ops.fwd_varlen(q, k, v, cu, 256, causal=True)
+    else:
+        ops.bwd_varlen(q, k, v, o, lse, do, cu, 256, causal=True)
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0x2001
+    assert ops.device_error() == 0
