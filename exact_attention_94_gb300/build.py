@@ -72,5 +72,31 @@ def build(verbose: bool = False, force: bool = False) -> str:
     return LIB
 
 
+COUNT_LIB = os.path.join(HERE, "libfa_count.so")
+
+
+def build_counting(verbose: bool = False) -> str:
+    """A test-only variant of the library: the forward kernel compiled with
+    FA_COUNT_RESCALES, which counts the lazy rescales it takes per (batch,
+    head) and exports fa_test_rescale_counts().  Linked from the product's
+    other objects; the product libfa.so never contains the counter."""
+    build(verbose=verbose)
+    obj = os.path.join(BUILD, "fa_fwd_count.o")
+    src = os.path.join(CSRC, "fa_fwd.cu")
+    nvcc = _nvcc()
+
+    def run(cmd):
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + r.stdout + r.stderr)
+
+    if _stale(obj, _deps(src)):
+        run([nvcc, *ARCH, *FLAGS, "-DFA_COUNT_RESCALES", "-c", src, "-o", obj])
+    objs = [obj if n == "fa_fwd.cu" else os.path.join(BUILD, os.path.splitext(n)[0] + ".o") for n in SOURCES]
+    if _stale(COUNT_LIB, objs):
+        run([nvcc, *ARCH, "-shared", "-o", COUNT_LIB, *objs])
+    return COUNT_LIB
+
+
 if __name__ == "__main__":
     print(build(verbose=True))

@@ -209,6 +209,18 @@ static bool window_ok(int& wl, int& wr, int max_len_q, int max_len_k) {
   return true;
 }
 
+// Grid rows of a packed batch's item list: an upper bound of the (sequence,
+// unit) items, sum_b ceil(len_b / unit) <= min(num_seqs * ceil(max_len / unit),
+// ceil(total / unit) + num_seqs).  0 (no list: the grid covers every sequence's
+// max_len) when the bound or the sequence count is too large for it.
+static int packed_items(int num_seqs, int units_max, int total_rows, int unit) {
+  const long long by_max = (long long)num_seqs * units_max;
+  const long long by_total = ((long long)total_rows + unit - 1) / unit + num_seqs;
+  const long long items = by_max < by_total ? by_max : by_total;
+  if (num_seqs > 2048 || items > 65535 || items < 1) return 0;
+  return (int)items;
+}
+
 static fa_status fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu,
                             const int* cu_k, int nbatch, int n_rows, int n_rows_k, int seq_len, int seq_len_k,
                             int max_len, int max_len_k, int H, int Hkv, int d, int wl, int wr, float scale,
@@ -243,6 +255,7 @@ static fa_status fwd_common(const void* q, const void* k, const void* v, void* o
   p.win_left = wl;
   p.win_right = wr;
   p.num_pairs = num_pairs;
+  p.num_items = cu ? packed_items(nbatch, num_pairs, n_rows, 256) : 0;
   p.max_len = max_len;
   p.max_len_k = max_len_k;
   p.scale_log2 = scale * kLog2e;
@@ -251,7 +264,7 @@ static fa_status fwd_common(const void* q, const void* k, const void* v, void* o
   p.timeout_ns = g_opt.timeout_ns;
   const int mk = mask_kind(wl, wr);
   const int poly = (mk == kMaskWindow && g_opt.poly != 0) ? 8 : g_opt.poly;
-  cudaError_t e = launch_fwd(tq, tk, tv, p, d, mk, poly, nbatch * H, (cudaStream_t)stream);
+  cudaError_t e = launch_fwd(tq, tk, tv, p, d, mk, poly, p.num_items > 0 ? H : nbatch * H, (cudaStream_t)stream);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
@@ -379,6 +392,7 @@ static fa_status bwd_common(const void* q, const void* k, const void* v, const v
   p.win_left = wl;
   p.win_right = wr;
   p.num_kblocks = num_kblocks;
+  p.num_items = cu ? packed_items(nbatch, num_kblocks, n_rows_k, 128) : 0;
   p.max_len = max_len;
   p.max_len_k = max_len_k;
   p.scale = scale;

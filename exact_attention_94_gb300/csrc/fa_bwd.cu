@@ -289,12 +289,25 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
 
   // one CTA per (batch, K/V head, key block); with grouped-query attention it
   // walks the query blocks of every query head that shares this K/V head
+  // Packed batches with an item list: y enumerates the (sequence, key block)
+  // items that exist and x, z the K/V heads.
   const int Hkv = p.H / p.kv_group;
-  const int bh = (int)(blockIdx.z * gridDim.x + blockIdx.x);
-  if (bh >= p.B * Hkv) return;
-  const int b = bh / Hkv;
-  const int h_kv = bh % Hkv;
-  const int jb = (int)blockIdx.y;
+  int b, h_kv, jb;
+  if (p.num_items > 0) {
+    h_kv = (int)(blockIdx.z * gridDim.x + blockIdx.x);
+    if (h_kv >= Hkv) return;
+    int units, total;
+    const bool found = varlen_item(p.cu_seqlens_k, p.B, 128, (int)blockIdx.y, b, jb, units, total);
+    if (blockIdx.y == gridDim.y - 1 && h_kv == 0 && total > (int)gridDim.y && threadIdx.x == 0 && p.err != nullptr)
+      atomicCAS(p.err, 0u, FA_DEVERR_BAD_SEQLEN);  // more items than the grid: the offsets are not as declared
+    if (!found) return;
+  } else {
+    const int bh = (int)(blockIdx.z * gridDim.x + blockIdx.x);
+    if (bh >= p.B * Hkv) return;
+    b = bh / Hkv;
+    h_kv = bh % Hkv;
+    jb = (int)blockIdx.y;
+  }
   const int k0 = jb * 128;
   const BwdItem it = bwd_item<MASK>(p, b, k0);
   if (it.bad) {
@@ -765,9 +778,10 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
   // set on every launch: the attribute belongs to the current device's context
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const int bh = p.B * (p.H / p.kv_group);  // CTAs walk (batch, K/V head) pairs
+  // CTAs walk (batch, K/V head) pairs, or K/V heads with an item list
+  const int bh = p.num_items > 0 ? p.H / p.kv_group : p.B * (p.H / p.kv_group);
   const int gx = bh < kBwdHeadGroup ? bh : kBwdHeadGroup;
-  dim3 grid(gx, p.num_kblocks, (bh + gx - 1) / gx);
+  dim3 grid(gx, p.num_items > 0 ? p.num_items : p.num_kblocks, (bh + gx - 1) / gx);
   kern<<<grid, kBwd128Threads, smem, stream>>>(tq, tk, tv, tdo, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -39,6 +39,14 @@
 
 namespace fa {
 
+#ifdef FA_COUNT_RESCALES
+// Test builds only (never the product library): rescales taken per (batch,
+// head), counted as the tiled model of the oracle counts them: a row's
+// reference maximum moves while an earlier one existed.
+constexpr int kCountSlots = 4096;
+__device__ unsigned long long g_rescale_count[kCountSlots];
+#endif
+
 namespace {
 
 template <int D, bool F8>
@@ -82,12 +90,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------------------------------------------------------- work item
   // grid: x = head within a group, y = query-tile pair (heaviest first), z = group of heads.
   // The block scheduler walks x fastest, so the CTAs in flight share a few heads' K/V in L2.
-  const int bh = (int)(blockIdx.z * gridDim.x + blockIdx.x);
-  if (bh >= p.bh_total) return;
-  const int b = bh / p.H;
-  const int h = bh % p.H;
+  // Packed batches with an item list: y enumerates the (sequence, pair) items that exist,
+  // each sequence's heaviest pair first, and x, z the heads, so no CTA is launched for
+  // the pairs a short sequence does not have.
+  int b, h, pair;
+  if (p.num_items > 0) {
+    h = (int)(blockIdx.z * gridDim.x + blockIdx.x);
+    if (h >= p.H) return;
+    int u, units, total;
+    const bool found = varlen_item(p.cu_seqlens, p.bh_total / p.H, 256, (int)blockIdx.y, b, u, units, total);
+    if (blockIdx.y == gridDim.y - 1 && h == 0 && total > (int)gridDim.y && threadIdx.x == 0 && p.err != nullptr)
+      atomicCAS(p.err, 0u, FA_DEVERR_BAD_SEQLEN);  // more items than the grid: the offsets are not as declared
+    if (!found) return;
+    pair = units - 1 - u;
+  } else {
+    const int bh = (int)(blockIdx.z * gridDim.x + blockIdx.x);
+    if (bh >= p.bh_total) return;
+    b = bh / p.H;
+    h = bh % p.H;
+    pair = p.num_pairs - 1 - (int)blockIdx.y;  // heaviest causal pairs first
+  }
   const int h_kv = h / p.kv_group;  // grouped-query attention: K/V head shared by kv_group query heads
-  const int pair = p.num_pairs - 1 - (int)blockIdx.y;  // heaviest causal pairs first
   int seq_start = 0, seq_len = p.seq_len, kv_start = 0, kv_len = p.seq_len_k, b_coord = b;
   if (p.cu_seqlens != nullptr) {
     seq_start = p.cu_seqlens[b];
@@ -312,6 +335,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + lane_off + 256u + (t ? (uint32_t)D : 0u);
     const float sl2 = p.scale_log2;
     const float tau = p.tau;
+#ifdef FA_COUNT_RESCALES
+    const int bh_count = b * p.H + h;
+#endif
     float m_ref = -INFINITY;
     float l = 0.f;
     bool ok = true;
@@ -384,6 +410,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_new = mx * sl2j;
       float alpha = 1.f;
       const bool resc = m_new > m_ref + tau;
+#ifdef FA_COUNT_RESCALES
+      if (resc && m_ref > -INFINITY && row < seq_len && bh_count < kCountSlots)
+        atomicAdd(&g_rescale_count[bh_count], 1ull);
+#endif
       if (resc) {
         alpha = ex2_sfu(m_ref - m_new);
         m_ref = m_new;
@@ -503,8 +533,9 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
   // or to race on between host threads).
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  // grid_x: (batch, head) units, or heads with an item list
   const int gx = grid_x < kHeadGroup ? grid_x : kHeadGroup;
-  dim3 grid(gx, p.num_pairs, (grid_x + gx - 1) / gx);
+  dim3 grid(gx, p.num_items > 0 ? p.num_items : p.num_pairs, (grid_x + gx - 1) / gx);
   kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
@@ -548,3 +579,13 @@ cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const C
 }
 
 }  // namespace fa
+
+#ifdef FA_COUNT_RESCALES
+// Test builds only: copies out (and clears) the per-(batch, head) rescale counts.
+extern "C" int fa_test_rescale_counts(unsigned long long* host, int n) {
+  if (n < 0 || n > fa::kCountSlots) return 1;
+  if (cudaMemcpyFromSymbol(host, fa::g_rescale_count, sizeof(unsigned long long) * n) != cudaSuccess) return 2;
+  static const unsigned long long zeros[fa::kCountSlots] = {};
+  return cudaMemcpyToSymbol(fa::g_rescale_count, zeros, sizeof(zeros)) == cudaSuccess ? 0 : 3;
+}
+#endif

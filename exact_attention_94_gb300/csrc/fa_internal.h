@@ -24,6 +24,9 @@ struct FwdParams {
   int win_left;              // mask (used by the masked kernels): query i sees keys
   int win_right;             //   [i + Nk - Nq - win_left, i + Nk - Nq + win_right]; -1 = unbounded side
   int num_pairs;             // grid.y: pairs of 128-row query tiles per (sequence, head)
+  int num_items;             // packed batch: grid.y enumerates (sequence, query-tile pair) items, the
+                             //   heaviest pair of each sequence first, and x, z the query heads; 0: grid
+                             //   over (batch, head) x pairs
   int max_len;               // longest query sequence the caller declared (packed: max_seqlen_q)
   int max_len_k;             // longest key sequence the caller declared
   // e4m3 operands only: one scale per 128-row block, [B][H][n_qblk] for Q and
@@ -62,6 +65,8 @@ struct BwdParams {
   int win_left;              // mask, as in FwdParams
   int win_right;
   int num_kblocks;           // grid.y of the main kernel
+  int num_items;             // packed batch: grid.y enumerates (sequence, key block) items and x, z the
+                             //   K/V heads; 0: grid over (batch, K/V head) x key blocks
   int max_len;               // longest query / key sequence the caller declared (packed calls)
   int max_len_k;
   float scale;

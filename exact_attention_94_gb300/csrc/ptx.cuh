@@ -378,6 +378,47 @@ __device__ __forceinline__ void ex2_poly2(float x0, float x1, float& y0, float& 
   y1 = __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23));
 }
 
+// Work items of a packed batch: sequence b (rows cu[b] .. cu[b+1]-1) has
+// ceil(len_b / unit) units (a negative length counts as one, so that the CTA
+// that gets it reports the bad offsets).  Maps item index y, which enumerates
+// the sequences' units in order, to (b, u, units of b); returns false past the
+// last unit.  *total receives the number of units of all sequences.  Called by
+// whole warps (every lane gets the result): 32 sequences per step, a shuffle
+// scan of their unit counts.
+__device__ __forceinline__ bool varlen_item(const int* cu, int num_seqs, int unit, int y, int& b, int& u,
+                                            int& units_b, int& total) {
+  const int lane = (int)(threadIdx.x & 31);
+  int base = 0;
+  bool found = false;
+  b = u = units_b = 0;
+  for (int c = 0; c < num_seqs; c += 32) {
+    const int s = c + lane;
+    int n = 0;
+    if (s < num_seqs) {
+      const int len = cu[s + 1] - cu[s];
+      n = len < 0 ? 1 : (len + unit - 1) / unit;
+    }
+    int incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const int chunk = __shfl_sync(0xffffffffu, incl, 31);
+    if (!found && y < base + chunk) {
+      const int l = __ffs(__ballot_sync(0xffffffffu, base + incl > y)) - 1;
+      const int incl_l = __shfl_sync(0xffffffffu, incl, l), n_l = __shfl_sync(0xffffffffu, n, l);
+      b = c + l;
+      u = y - (base + incl_l - n_l);
+      units_b = n_l;
+      found = true;
+    }
+    base += chunk;
+  }
+  total = base;
+  return found;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
