@@ -12,6 +12,7 @@ LIB_PATH = os.path.join(HERE, "libfa.so")
 FA_BWD_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 FA_DEVERR_SELFTEST_CODE = 0x10FF
 FA_OPT_RESCALE_TAU, FA_OPT_POLY_EXP, FA_OPT_WAIT_TIMEOUT_MS = 1, 2, 3
+FA_POLY_EXP_DEFAULT = 16  # the library's default share of exponentials on the cubic: one column pair in 16
 
 # every symbol include/fa.h declares, with (restype, argtypes)
 _P = ctypes.c_void_p

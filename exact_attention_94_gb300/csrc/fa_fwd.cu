@@ -24,7 +24,8 @@
 // 2^floor(x) * p3(x - floor(x)) with a cubic fitted in fit_exp2_poly.py: one
 // column pair in POLYK (template argument; 0 = none) goes to the cubic.
 //
-// CTA organisation (one CTA per pair of 128-row query tiles of one head):
+// CTA organisation (one CTA per couple of 256-row query chunks of one head,
+// each chunk a pair of 128-row query tiles, computed one after the other):
 //   warp 0      TMA producer: Q tiles once, then K_j, V_j into a ring of slots
 //   warp 1      allocates TMEM and runs the MMA loop; an elect.sync lane issues each tcgen05.mma
 //   warps 4-7   softmax of query tile 0 (thread = row = TMEM lane)
@@ -87,28 +88,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = warp_id();
   const int lane = lane_id();
 
-  // ---------------------------------------------------------------- work item
-  // grid: x = head within a group, y = query-tile pair (heaviest first), z = group of heads.
-  // The block scheduler walks x fastest, so the CTAs in flight share a few heads' K/V in L2.
-  // Packed batches with an item list: y enumerates the (sequence, pair) items that exist,
-  // each sequence's heaviest pair first, and x, z the heads, so no CTA is launched for
-  // the pairs a short sequence does not have.
-  int b, h, pair;
+  // ---------------------------------------------------------------- work
+  // A CTA computes one 256-row query chunk (a pair of 128-row tiles) of one
+  // (sequence, head), or, when p.couple is set, two: chunks P-1-u and u of a
+  // sequence with P chunks, one after the other, the second one's Q loading
+  // while the first one's last products run and the first one's epilogue
+  // overlapping the second one's first scores.  Single chunks go heaviest
+  // first (chunk P-1-u for CTA u), which packs the tail of a causal grid
+  // best; couples halve the CTAs' start and end costs where those weigh more
+  // (short or unmasked sequences).  grid: x = head within a group, y = u, z =
+  // group of heads (the block scheduler walks x fastest, so the CTAs in flight
+  // share a few heads' K/V in L2).  Packed batches with an item list: y
+  // enumerates the (sequence, u) items that exist and x, z the heads, so no
+  // CTA is launched for the chunks a short sequence does not have.
+  int b, h, u;
   if (p.num_items > 0) {
     h = (int)(blockIdx.z * gridDim.x + blockIdx.x);
     if (h >= p.H) return;
-    int u, units, total;
-    const bool found = varlen_item(p.cu_seqlens, p.bh_total / p.H, 256, (int)blockIdx.y, b, u, units, total);
+    int units, total;
+    const bool found =
+        varlen_item(p.cu_seqlens, p.bh_total / p.H, p.couple ? 512 : 256, (int)blockIdx.y, b, u, units, total);
     if (blockIdx.y == gridDim.y - 1 && h == 0 && total > (int)gridDim.y && threadIdx.x == 0 && p.err != nullptr)
       atomicCAS(p.err, 0u, FA_DEVERR_BAD_SEQLEN);  // more items than the grid: the offsets are not as declared
     if (!found) return;
-    pair = units - 1 - u;
   } else {
     const int bh = (int)(blockIdx.z * gridDim.x + blockIdx.x);
     if (bh >= p.bh_total) return;
     b = bh / p.H;
     h = bh % p.H;
-    pair = p.num_pairs - 1 - (int)blockIdx.y;  // heaviest causal pairs first
+    u = (int)blockIdx.y;
   }
   const int h_kv = h / p.kv_group;  // grouped-query attention: K/V head shared by kv_group query heads
   int seq_start = 0, seq_len = p.seq_len, kv_start = 0, kv_len = p.seq_len_k, b_coord = b;
@@ -125,37 +133,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       return;
     }
   }
-  const int q0 = pair * 256;
-  if (q0 >= seq_len) return;  // uniform for the CTA, before any shared state exists
+  const int n_chunks = (seq_len + 255) / 256;
+  if (u >= (p.couple ? (n_chunks + 1) / 2 : n_chunks)) return;  // uniform for the CTA, before any shared state
+  const int n_items = (!p.couple || n_chunks - 1 - u == u) ? 1 : 2;
+  auto chunk_of = [&](int it) { return it == 0 ? n_chunks - 1 - u : u; };
 
-  // Key tiles each query tile t visits: [jlo_t, jhi_t).  A tile's rows see
-  // keys [key_lo(first row), key_hi(last row)) between them (both bounds grow
-  // with the row), so the tiles outside that range are skipped entirely.
-  auto tile_range = [&](int t, int& lo_t, int& hi_t) {
-    const int r0 = q0 + 128 * t;
-    lo_t = hi_t = 0;
-    if (r0 < seq_len) {
-      const int r1 = min(r0 + 127, seq_len - 1);
-      const int lo = LEFT ? mask_key_lo(r0, seq_len, kv_len, p.win_left) : 0;
-      const int hi = MASKED ? mask_key_hi(r1, seq_len, kv_len, p.win_right) : kv_len;
-      if (hi > lo) {
-        lo_t = lo / 128;
-        hi_t = (hi + 127) / 128;
+  // Key tiles query tile t of chunk `chunk` visits: [lo_t, hi_t).  A tile's rows
+  // see keys [key_lo(first row), key_hi(last row)) between them (both bounds
+  // grow with the row), so the tiles outside that range are skipped entirely.
+  // The producer streams the union of the two tiles' ranges, which is
+  // contiguous (tile 1 starts no later than tile 0 ends: window_left +
+  // window_right >= 0).
+  auto ranges_of = [&](int chunk, int& lo0, int& hi0, int& lo1, int& hi1, int& jmin, int& jmax) {
+    int lo_t[2], hi_t[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const int r0 = chunk * 256 + 128 * t;
+      lo_t[t] = hi_t[t] = 0;
+      if (r0 < seq_len) {
+        const int r1 = min(r0 + 127, seq_len - 1);
+        const int lo = LEFT ? mask_key_lo(r0, seq_len, kv_len, p.win_left) : 0;
+        const int hi = MASKED ? mask_key_hi(r1, seq_len, kv_len, p.win_right) : kv_len;
+        if (hi > lo) {
+          lo_t[t] = lo / 128;
+          hi_t[t] = (hi + 127) / 128;
+        }
       }
     }
+    lo0 = lo_t[0], hi0 = hi_t[0], lo1 = lo_t[1], hi1 = hi_t[1];
+    const bool live0 = hi0 > lo0, live1 = hi1 > lo1;
+    jmin = live0 ? lo0 : lo1;
+    jmax = live1 ? hi1 : hi0;
   };
-  int jlo0, jhi0, jlo1, jhi1;
-  tile_range(0, jlo0, jhi0);
-  tile_range(1, jlo1, jhi1);
-  // The producer streams the union of the two ranges; it is contiguous, since
-  // tile 1 starts no later than tile 0 ends (window_left + window_right >= 0).
-  const bool live0 = jhi0 > jlo0, live1 = jhi1 > jlo1;
-  const int jmin = live0 ? jlo0 : jlo1;
-  const int jmax = live1 ? jhi1 : jhi0;
 
   // ---------------------------------------------------------------- barriers
-  enum { Q_FULL = 0, KV_FULL = 1, KV_EMPTY = 1 + NS, S_FULL = 1 + 2 * NS, P_FULL = S_FULL + 2, O_FINAL = P_FULL + 2,
-         DRAIN = O_FINAL + 2, NBARS = DRAIN + 1 };
+  // Per chunk: Q_FULL (Q landed), Q_EMPTY (its last S product done: the Q
+  // buffer is free), O_FINAL[t] (tile t's last P V product done; only chunks
+  // where tile t sees keys), O_EMPTY[t] (tile t's epilogue has read O).  Per
+  // visited key tile: S_FULL[t], P_FULL[t], and the K/V ring's FULL/EMPTY
+  // slots, whose counts continue from one chunk to the next.
+  enum { Q_FULL = 0, Q_EMPTY = 1, KV_FULL = 2, KV_EMPTY = 2 + NS, S_FULL = 2 + 2 * NS, P_FULL = S_FULL + 2,
+         O_FINAL = P_FULL + 2, O_EMPTY = O_FINAL + 2, DRAIN = O_EMPTY + 2, NBARS = DRAIN + 1 };
+  static_assert(8 * NBARS + 8 <= 256, "barrier area");
   const uint32_t bar0 = base + L::kBarOff;
   auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + L::kBarOff + 8 * NBARS);
@@ -163,6 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(Q_FULL), 1);
+    mbar_init(BAR(Q_EMPTY), 1);
     for (int i = 0; i < NS; ++i) {
       mbar_init(BAR(KV_FULL + i), 1);
       mbar_init(BAR(KV_EMPTY + i), 1);
@@ -171,6 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(BAR(S_FULL + t), 1);
       mbar_init(BAR(P_FULL + t), 128);
       mbar_init(BAR(O_FINAL + t), 1);
+      mbar_init(BAR(O_EMPTY + t), 128);
     }
     mbar_init(BAR(DRAIN), 1);
     *abort_flag = 0;
@@ -195,30 +216,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(BAR(Q_FULL), 2 * TILE);
-      for (int t = 0; t < 2; ++t)
-        for (int c = 0; c < CH; ++c)
-          tma_load_4d(q_s + t * TILE + c * CHUNK, &tm_q, BAR(Q_FULL), c * CHUNK_ELEMS, seq_start + q0 + 128 * t, h,
-                      b_coord);
       bool ok = true;
-      for (int j = jmin; j < jmax && ok; ++j) {
-        for (int which = 0; which < 2; ++which) {
-          const int u = 2 * (j - jmin) + which;
-          const int slot = u % NS;
-          if (u >= NS && !mbar_wait(BAR(KV_EMPTY + slot), ((u / NS) - 1) & 1, w, 1)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(BAR(KV_FULL + slot), TILE);
-          if (F8 && which) {  // V^T codes: d rows of 128 keys
-            tma_load_4d(kv_s + slot * TILE, &tm_v, BAR(KV_FULL + slot), 128 * j, 0, h_kv, b_coord);
-            continue;
-          }
-          const CUtensorMap* m = which ? &tm_v : &tm_k;
+      int ring = 0;  // K/V ring positions used by earlier chunks
+      for (int it = 0; it < n_items && ok; ++it) {
+        const int q0 = chunk_of(it) * 256;
+        int lo0, hi0, lo1, hi1, jmin, jmax;
+        ranges_of(chunk_of(it), lo0, hi0, lo1, hi1, jmin, jmax);
+        // the previous chunk's S products must be done with the Q buffer
+        if (it > 0 && !(ok = mbar_wait(BAR(Q_EMPTY), (it - 1) & 1, w, 9))) break;
+        mbar_arrive_expect_tx(BAR(Q_FULL), 2 * TILE);
+        for (int t = 0; t < 2; ++t)
           for (int c = 0; c < CH; ++c)
-            tma_load_4d(kv_s + slot * TILE + c * CHUNK, m, BAR(KV_FULL + slot), c * CHUNK_ELEMS, kv_start + 128 * j,
-                        h_kv, b_coord);
+            tma_load_4d(q_s + t * TILE + c * CHUNK, &tm_q, BAR(Q_FULL), c * CHUNK_ELEMS, seq_start + q0 + 128 * t, h,
+                        b_coord);
+        for (int j = jmin; j < jmax && ok; ++j) {
+          for (int which = 0; which < 2; ++which) {
+            const int uu = ring + 2 * (j - jmin) + which;
+            const int slot = uu % NS;
+            if (uu >= NS && !mbar_wait(BAR(KV_EMPTY + slot), ((uu / NS) - 1) & 1, w, 1)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(BAR(KV_FULL + slot), TILE);
+            if (F8 && which) {  // V^T codes: d rows of 128 keys
+              tma_load_4d(kv_s + slot * TILE, &tm_v, BAR(KV_FULL + slot), 128 * j, 0, h_kv, b_coord);
+              continue;
+            }
+            const CUtensorMap* m = which ? &tm_v : &tm_k;
+            for (int c = 0; c < CH; ++c)
+              tma_load_4d(kv_s + slot * TILE + c * CHUNK, m, BAR(KV_FULL + slot), c * CHUNK_ELEMS,
+                          kv_start + 128 * j, h_kv, b_coord);
+          }
         }
+        ring += 2 * (jmax - jmin);
       }
       if (!ok) {  // let copies already in flight land before the CTA's shared memory goes away
         const uint64_t t0 = globaltimer_ns();
@@ -268,54 +298,80 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
 
-      ok = __all_sync(0xffffffffu, mbar_wait(BAR(Q_FULL), 0, w, 2));
-      tc_fence_after();
-      // Ring position u of key tile j is 2 (j - jmin) (K) and 2 (j - jmin) + 1 (V);
-      // tile t's S / P barriers complete once per visited key tile, phase j - jlo_t.
-      for (int j = jmin; j < jmax && ok; ++j) {
-        const int uk = 2 * (j - jmin), sk = uk % NS;
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(KV_FULL + sk), (uk / NS) & 1, w, 3)))) break;
+      int ring = 0;                 // K/V ring positions used by earlier chunks
+      int sph0 = 0, sph1 = 0;       // S / P phases of each tile used by earlier chunks
+      for (int it = 0; it < n_items && ok; ++it) {
+        int jlo0, jhi0, jlo1, jhi1, jmin, jmax;
+        ranges_of(chunk_of(it), jlo0, jhi0, jlo1, jhi1, jmin, jmax);
+        // The first P V product of tile t overwrites O_t: the previous chunk's epilogue must have read it.
+        auto first_pv_wait = [&](int t) -> bool {
+          if (it == 0) return true;
+          const bool good = __all_sync(0xffffffffu, mbar_wait(BAR(O_EMPTY + t), (it - 1) & 1, w, 10));
+          if (good) tc_fence_after();
+          return good;
+        };
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(Q_FULL), it & 1, w, 2)))) break;
         tc_fence_after();
-        if (j >= jlo0 && j < jhi0) {
-          issue_S(0, sk);
-          mma_commit_w(BAR(S_FULL + 0));
-        }
-        if (j > jmin) {
-          const int sv = (uk - 1) % NS;
-          if (j - 1 >= jlo1 && j - 1 < jhi1) {
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(P_FULL + 1), (j - 1 - jlo1) & 1, w, 4)))) break;
-            tc_fence_after();
-            issue_PV(1, sv, j - 1 > jlo1);
-            if (j - 1 == jhi1 - 1) mma_commit_w(BAR(O_FINAL + 1));
-          }
-          mma_commit_w(BAR(KV_EMPTY + sv));
-        }
-        if (j >= jlo1 && j < jhi1) {
-          issue_S(1, sk);
-          mma_commit_w(BAR(S_FULL + 1));
-        }
-        mma_commit_w(BAR(KV_EMPTY + sk));
-        const int uv = uk + 1, sv = uv % NS;
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(KV_FULL + sv), (uv / NS) & 1, w, 5)))) break;
-        tc_fence_after();
-        if (j >= jlo0 && j < jhi0) {
-          if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(P_FULL + 0), (j - jlo0) & 1, w, 6)))) break;
+        // Ring position u of key tile j is ring + 2 (j - jmin) (K) and + 1 (V);
+        // tile t's S / P barriers complete once per visited key tile.
+        for (int j = jmin; j < jmax && ok; ++j) {
+          const int uk = ring + 2 * (j - jmin), sk = uk % NS;
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(KV_FULL + sk), (uk / NS) & 1, w, 3)))) break;
           tc_fence_after();
-          issue_PV(0, sv, j > jlo0);
-          if (j == jhi0 - 1) mma_commit_w(BAR(O_FINAL + 0));
-        }
-      }
-      if (ok && jmax > jmin) {
-        const int j = jmax;
-        const int sv = (2 * (j - 1 - jmin) + 1) % NS;
-        if (j - 1 >= jlo1 && j - 1 < jhi1) {
-          if ((ok = __all_sync(0xffffffffu, mbar_wait(BAR(P_FULL + 1), (j - 1 - jlo1) & 1, w, 4)))) {
+          if (j >= jlo0 && j < jhi0) {
+            issue_S(0, sk);
+            mma_commit_w(BAR(S_FULL + 0));
+          }
+          if (j > jmin) {
+            const int sv = (uk - 1) % NS;
+            if (j - 1 >= jlo1 && j - 1 < jhi1) {
+              if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(P_FULL + 1), (sph1 + j - 1 - jlo1) & 1, w, 4))))
+                break;
+              tc_fence_after();
+              if (j - 1 == jlo1 && !(ok = first_pv_wait(1))) break;
+              issue_PV(1, sv, j - 1 > jlo1);
+              if (j - 1 == jhi1 - 1) mma_commit_w(BAR(O_FINAL + 1));
+            }
+            mma_commit_w(BAR(KV_EMPTY + sv));
+          }
+          if (j >= jlo1 && j < jhi1) {
+            issue_S(1, sk);
+            mma_commit_w(BAR(S_FULL + 1));
+          }
+          // the chunk's last S product: the Q buffer is free once it is done
+          if (j == jmax - 1) mma_commit_w(BAR(Q_EMPTY));
+          mma_commit_w(BAR(KV_EMPTY + sk));
+          const int uv = uk + 1, sv = uv % NS;
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(KV_FULL + sv), (uv / NS) & 1, w, 5)))) break;
+          tc_fence_after();
+          if (j >= jlo0 && j < jhi0) {
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(P_FULL + 0), (sph0 + j - jlo0) & 1, w, 6))))
+              break;
             tc_fence_after();
-            issue_PV(1, sv, j - 1 > jlo1);
-            mma_commit_w(BAR(O_FINAL + 1));
+            if (j == jlo0 && !(ok = first_pv_wait(0))) break;
+            issue_PV(0, sv, j > jlo0);
+            if (j == jhi0 - 1) mma_commit_w(BAR(O_FINAL + 0));
           }
         }
-        if (ok) mma_commit_w(BAR(KV_EMPTY + sv));
+        if (ok && jmax > jmin) {
+          const int j = jmax;
+          const int sv = (ring + 2 * (j - 1 - jmin) + 1) % NS;
+          if (j - 1 >= jlo1 && j - 1 < jhi1) {
+            if ((ok = __all_sync(0xffffffffu, mbar_wait(BAR(P_FULL + 1), (sph1 + j - 1 - jlo1) & 1, w, 4)))) {
+              tc_fence_after();
+              if (j - 1 == jlo1) ok = first_pv_wait(1);
+              if (ok) {
+                issue_PV(1, sv, j - 1 > jlo1);
+                mma_commit_w(BAR(O_FINAL + 1));
+              }
+            }
+          }
+          if (ok) mma_commit_w(BAR(KV_EMPTY + sv));
+        }
+        if (ok && jmax <= jmin) mma_commit_w(BAR(Q_EMPTY));  // a chunk with no key tile: nothing read Q
+        ring += 2 * (jmax - jmin);
+        sph0 += jhi0 - jlo0;
+        sph1 += jhi1 - jlo1;
       }
       // Drain: every product and every earlier commit's arrival has landed
       // before TMEM is released and the CTA's shared memory goes away.
@@ -329,7 +385,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = (warp - 4) >> 2;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
-    const int row = q0 + 128 * t + r;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + (t ? 128u : 0u);
     const uint32_t tO = tmem + lane_off + 256u + (t ? (uint32_t)D : 0u);
@@ -338,25 +393,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #ifdef FA_COUNT_RESCALES
     const int bh_count = b * p.H + h;
 #endif
-    float m_ref = -INFINITY;
-    float l = 0.f;
     bool ok = true;
-    // keys this row sees: [key_lo, key_hi)
-    const int key_lo = LEFT ? mask_key_lo(row, seq_len, kv_len, p.win_left) : 0;
-    const int key_hi = MASKED ? mask_key_hi(row, seq_len, kv_len, p.win_right) : kv_len;
-    const int jlo = t ? jlo1 : jlo0, jhi = t ? jhi1 : jhi0;
     // e4m3 operands: scores of key tile j are dequantised by sq (this query
     // tile's scale) * sk_j; P of tile j is multiplied by sv_j / sv_ref before
     // its rounding to e4m3 (sv_ref = the head's largest V scale, so P stays in
     // [0, 2^tau]) and O by sv_ref at the end.  The factor goes into the
     // exponent, and l adds P back at its own scale.
-    float sl2_q = sl2, sv_ref = 1.f;
+    float sv_ref = 1.f;
     const float* k_sc = nullptr;
     const float* v_sc = nullptr;
     if constexpr (F8) {
       const size_t hk = (size_t)b * (p.H / p.kv_group) + h_kv;
-      const int qb = (q0 >> 7) + t;  // past the last block only when this tile has no rows
-      sl2_q = qb < p.n_qblk ? sl2 * p.q_scale[((size_t)b * p.H + h) * p.n_qblk + qb] : 0.f;
       k_sc = p.k_scale + hk * p.n_kblk;
       v_sc = p.v_scale + hk * p.n_kblk;
       float mv = 0.f;
@@ -365,133 +412,156 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int o = 16; o > 0; o >>= 1) mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, o));
       sv_ref = mv > 0.f ? mv : 1.f;
     }
-
-    for (int j = jlo; j < jhi; ++j) {
-      float sl2j = sl2, lrv = 0.f, inv_rv = 1.f;
+    int sphase = 0;  // S / P phases of this tile used by earlier chunks
+    int nfinal = 0;  // O_FINAL phases of this tile used by earlier chunks
+    for (int it = 0; it < n_items && ok; ++it) {
+      const int q0 = chunk_of(it) * 256;
+      int lo0, hi0, lo1, hi1, jmin_, jmax_;
+      ranges_of(chunk_of(it), lo0, hi0, lo1, hi1, jmin_, jmax_);
+      const int row = q0 + 128 * t + r;
+      float m_ref = -INFINITY;
+      float l = 0.f;
+      // keys this row sees: [key_lo, key_hi)
+      const int key_lo = LEFT ? mask_key_lo(row, seq_len, kv_len, p.win_left) : 0;
+      const int key_hi = MASKED ? mask_key_hi(row, seq_len, kv_len, p.win_right) : kv_len;
+      const int jlo = t ? lo1 : lo0, jhi = t ? hi1 : hi0;
+      float sl2_q = sl2;
       if constexpr (F8) {
-        // an all-zero Q or K block (scale 0) has all-zero codes, so its scores are
-        // exactly 0 under any positive multiplier; a positive one keeps masked
-        // -inf scores at -inf instead of turning them into NaN
-        sl2j = fmaxf(sl2_q * k_sc[j], 1e-30f);
-        const float rv = fmaxf(v_sc[j] / sv_ref, 0x1p-30f);  // a zero block's P rounds to 0 either way
-        lrv = log2f(rv);
-        inv_rv = 1.f / rv;
+        const int qb = (q0 >> 7) + t;  // past the last block only when this tile has no rows
+        sl2_q = qb < p.n_qblk ? sl2 * p.q_scale[((size_t)b * p.H + h) * p.n_qblk + qb] : 0.f;
       }
-      ok = mbar_wait(BAR(S_FULL + t), (j - jlo) & 1, w, 7);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sr[c]);
-      tmem_ld_wait();
-      float x[128];
-#pragma unroll
-      for (int i = 0; i < 128; ++i) x[i] = __uint_as_float(sr[i / 32][i % 32]);
 
-      const int kv0 = 128 * j;
-      if ((LEFT && kv0 < key_lo) || kv0 + 128 > key_hi) {
-#pragma unroll
-        for (int i = 0; i < 128; ++i)
-          if ((LEFT && kv0 + i < key_lo) || kv0 + i >= key_hi) x[i] = -INFINITY;
-      }
-      // row maximum: eight short chains of 3-input maxima, then a small tree
-      float mg[8];
-#pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        float m = fmaxf(x[16 * g], x[16 * g + 1]);
-#pragma unroll
-        for (int i = 2; i < 16; i += 2) m = max3f(m, x[16 * g + i], x[16 * g + i + 1]);
-        mg[g] = m;
-      }
-      const float mx = max3f(max3f(mg[0], mg[1], mg[2]), max3f(mg[3], mg[4], mg[5]), fmaxf(mg[6], mg[7]));
-      const float m_new = mx * sl2j;
-      float alpha = 1.f;
-      const bool resc = m_new > m_ref + tau;
-#ifdef FA_COUNT_RESCALES
-      if (resc && m_ref > -INFINITY && row < seq_len && bh_count < kCountSlots)
-        atomicAdd(&g_rescale_count[bh_count], 1ull);
-#endif
-      if (resc) {
-        alpha = ex2_sfu(m_ref - m_new);
-        m_ref = m_new;
-      }
-      const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
-
-      // p = 2^(x * scale * log2 e - m_ref): packed FMA, exponentials, packed partial sums
-      const uint64_t sl2x2 = f2_pack(sl2j, sl2j);
-      const uint64_t nmb2 = f2_pack(lrv - mb, lrv - mb);
-      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-      uint32_t pk[2][32];
-      float ph0 = 0.f, ph1 = 0.f;  // e4m3: the previous pair, packed with the next into one word
-#pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        float y0, y1;
-        f2_unpack(f2_fma(f2_pack(x[2 * i], x[2 * i + 1]), sl2x2, nmb2), y0, y1);
-        float p0, p1;
-        if (POLYK > 0 && (i % POLYK) == POLYK - 1) {
-          ex2_poly2(y0, y1, p0, p1);
-        } else {
-          p0 = ex2_sfu(y0);
-          p1 = ex2_sfu(y1);
-        }
-        acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
+      for (int j = jlo; j < jhi; ++j) {
+        float sl2j = sl2, lrv = 0.f, inv_rv = 1.f;
         if constexpr (F8) {
-          if (i & 1)
-            pk[0][i / 2] = pack_e4m3x4(ph0, ph1, p0, p1);  // keys 4c..4c+3 in column c
-          else
-            ph0 = p0, ph1 = p1;
-        } else {
-          pk[i / 32][i % 32] = pack_bf16x2(p0, p1);
-          if (i == 31) tmem_st32(tS, pk[0]);  // first half of P out early: frees registers
+          // an all-zero Q or K block (scale 0) has all-zero codes, so its scores are
+          // exactly 0 under any positive multiplier; a positive one keeps masked
+          // -inf scores at -inf instead of turning them into NaN
+          sl2j = fmaxf(sl2_q * k_sc[j], 1e-30f);
+          const float rv = fmaxf(v_sc[j] / sv_ref, 0x1p-30f);  // a zero block's P rounds to 0 either way
+          lrv = log2f(rv);
+          inv_rv = 1.f / rv;
         }
-      }
-      float s0, s1, s2, s3, s4, s5, s6, s7;
-      f2_unpack(acc[0], s0, s1);
-      f2_unpack(acc[1], s2, s3);
-      f2_unpack(acc[2], s4, s5);
-      f2_unpack(acc[3], s6, s7);
-      l = l * alpha + (((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7))) * inv_rv;
-
-      if (j > jlo && __any_sync(0xffffffffu, resc)) {
-        // rows whose reference moved: O~ *= alpha (alpha = 1 for the others)
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t ov[32];
-          tmem_ld32(tO + 32 * c, ov);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-          tmem_st32(tO + 32 * c, ov);
+        ok = mbar_wait(BAR(S_FULL + t), (sphase + j - jlo) & 1, w, 7);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
         }
-      }
-      if constexpr (F8)
-        tmem_st32(tS, pk[0]);  // the whole tile's P: 32 columns of four e4m3 each
-      else
-        tmem_st32(tS + 32, pk[1]);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(BAR(P_FULL + t));
-    }
+        tc_fence_after();
+        uint32_t sr[4][32];
+  #pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sr[c]);
+        tmem_ld_wait();
+        float x[128];
+  #pragma unroll
+        for (int i = 0; i < 128; ++i) x[i] = __uint_as_float(sr[i / 32][i % 32]);
 
-    // ------------------------------------------------------------ epilogue
-    const bool row_ok = row < seq_len;
-    __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) +
-                          (((size_t)b_coord * p.n_rows + seq_start + row) * p.H + h) * D;
-    float* lse_out = p.lse + ((size_t)b_coord * p.H + h) * p.n_rows + seq_start + row;
-    if (jhi <= jlo) {
-      // no key tile visible to any row of this tile: O = 0, lse = -inf
-      if (row_ok) {
-        uint4* dst = reinterpret_cast<uint4*>(orow);
-#pragma unroll
-        for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
-        *lse_out = -INFINITY;
+        const int kv0 = 128 * j;
+        if ((LEFT && kv0 < key_lo) || kv0 + 128 > key_hi) {
+  #pragma unroll
+          for (int i = 0; i < 128; ++i)
+            if ((LEFT && kv0 + i < key_lo) || kv0 + i >= key_hi) x[i] = -INFINITY;
+        }
+        // row maximum: eight short chains of 3-input maxima, then a small tree
+        float mg[8];
+  #pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          float m = fmaxf(x[16 * g], x[16 * g + 1]);
+  #pragma unroll
+          for (int i = 2; i < 16; i += 2) m = max3f(m, x[16 * g + i], x[16 * g + i + 1]);
+          mg[g] = m;
+        }
+        const float mx = max3f(max3f(mg[0], mg[1], mg[2]), max3f(mg[3], mg[4], mg[5]), fmaxf(mg[6], mg[7]));
+        const float m_new = mx * sl2j;
+        float alpha = 1.f;
+        const bool resc = m_new > m_ref + tau;
+  #ifdef FA_COUNT_RESCALES
+        if (resc && m_ref > -INFINITY && row < seq_len && bh_count < kCountSlots)
+          atomicAdd(&g_rescale_count[bh_count], 1ull);
+  #endif
+        if (resc) {
+          alpha = ex2_sfu(m_ref - m_new);
+          m_ref = m_new;
+        }
+        const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
+
+        // p = 2^(x * scale * log2 e - m_ref): packed FMA, exponentials, packed partial sums
+        const uint64_t sl2x2 = f2_pack(sl2j, sl2j);
+        const uint64_t nmb2 = f2_pack(lrv - mb, lrv - mb);
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+        uint32_t pk[2][32];
+        float ph0 = 0.f, ph1 = 0.f;  // e4m3: the previous pair, packed with the next into one word
+  #pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          float y0, y1;
+          f2_unpack(f2_fma(f2_pack(x[2 * i], x[2 * i + 1]), sl2x2, nmb2), y0, y1);
+          float p0, p1;
+          if (POLYK > 0 && (i % (POLYK > 0 ? POLYK : 1)) == POLYK - 1) {
+            ex2_poly2(y0, y1, p0, p1);
+          } else {
+            p0 = ex2_sfu(y0);
+            p1 = ex2_sfu(y1);
+          }
+          acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
+          if constexpr (F8) {
+            if (i & 1)
+              pk[0][i / 2] = pack_e4m3x4(ph0, ph1, p0, p1);  // keys 4c..4c+3 in column c
+            else
+              ph0 = p0, ph1 = p1;
+          } else {
+            pk[i / 32][i % 32] = pack_bf16x2(p0, p1);
+            if (i == 31) tmem_st32(tS, pk[0]);  // first half of P out early: frees registers
+          }
+        }
+        float s0, s1, s2, s3, s4, s5, s6, s7;
+        f2_unpack(acc[0], s0, s1);
+        f2_unpack(acc[1], s2, s3);
+        f2_unpack(acc[2], s4, s5);
+        f2_unpack(acc[3], s6, s7);
+        l = l * alpha + (((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7))) * inv_rv;
+
+        if (j > jlo && __any_sync(0xffffffffu, resc)) {
+          // rows whose reference moved: O~ *= alpha (alpha = 1 for the others)
+  #pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(tO + 32 * c, ov);
+            tmem_ld_wait();
+  #pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            tmem_st32(tO + 32 * c, ov);
+          }
+        }
+        if constexpr (F8)
+          tmem_st32(tS, pk[0]);  // the whole tile's P: 32 columns of four e4m3 each
+        else
+          tmem_st32(tS + 32, pk[1]);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(BAR(P_FULL + t));
       }
-    } else if (ok) {
-      ok = mbar_wait(BAR(O_FINAL + t), 0, w, 8);
-      if (__all_sync(0xffffffffu, ok)) {
+      sphase += jhi - jlo;
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue of the chunk
+      const bool row_ok = row < seq_len;
+      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) +
+                            (((size_t)b_coord * p.n_rows + seq_start + row) * p.H + h) * D;
+      float* lse_out = p.lse + ((size_t)b_coord * p.H + h) * p.n_rows + seq_start + row;
+      if (jhi <= jlo) {
+        // no key tile visible to any row of this tile: O = 0, lse = -inf
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+          for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+          *lse_out = -INFINITY;
+        }
+      } else {
+        ok = mbar_wait(BAR(O_FINAL + t), nfinal & 1, w, 8);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        ++nfinal;
         tc_fence_after();
         const float inv_l = l > 0.f ? sv_ref / l : 0.f;  // sv_ref = 1 unless e4m3
 #pragma unroll
@@ -511,6 +581,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (row_ok) *lse_out = l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
       }
+      // O has been read: the next chunk's first P V product may overwrite it
+      tc_fence_before();
+      mbar_arrive(BAR(O_EMPTY + t));
     }
   }
 
@@ -535,7 +608,9 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
   if (e != cudaSuccess) return e;
   // grid_x: (batch, head) units, or heads with an item list
   const int gx = grid_x < kHeadGroup ? grid_x : kHeadGroup;
-  dim3 grid(gx, p.num_items > 0 ? p.num_items : p.num_pairs, (grid_x + gx - 1) / gx);
+  // y: 256-row query chunks (or couples of them), or the packed batch's items
+  dim3 grid(gx, p.num_items > 0 ? p.num_items : (p.couple ? (p.num_pairs + 1) / 2 : p.num_pairs),
+            (grid_x + gx - 1) / gx);
   kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }

@@ -23,10 +23,10 @@ struct FwdParams {
   int seq_len_k;             // dense: Nk
   int win_left;              // mask (used by the masked kernels): query i sees keys
   int win_right;             //   [i + Nk - Nq - win_left, i + Nk - Nq + win_right]; -1 = unbounded side
-  int num_pairs;             // grid.y: pairs of 128-row query tiles per (sequence, head)
-  int num_items;             // packed batch: grid.y enumerates (sequence, query-tile pair) items, the
-                             //   heaviest pair of each sequence first, and x, z the query heads; 0: grid
-                             //   over (batch, head) x pairs
+  int num_pairs;             // 256-row query chunks (pairs of 128-row tiles) of the longest sequence
+  int couple;                // 1: a CTA computes two chunks of a (sequence, head), P-1-u and u
+  int num_items;             // packed batch: grid.y enumerates (sequence, chunk or couple) items and x, z
+                             //   the query heads; 0: grid over (batch, head) x chunks (or couples)
   int max_len;               // longest query sequence the caller declared (packed: max_seqlen_q)
   int max_len_k;             // longest key sequence the caller declared
   // e4m3 operands only: one scale per 128-row block, [B][H][n_qblk] for Q and

@@ -86,7 +86,7 @@ def test_options(lib):
         assert lib.fa_set_option(_lib.FA_OPT_POLY_EXP, share) == _lib.FA_OK
     for share in (2.0, 3.0, -1.0, 32.0):
         assert lib.fa_set_option(_lib.FA_OPT_POLY_EXP, share) == _lib.FA_ERR_INVALID_ARG
-    assert lib.fa_set_option(_lib.FA_OPT_POLY_EXP, 0.0) == _lib.FA_OK
+    assert lib.fa_set_option(_lib.FA_OPT_POLY_EXP, _lib.FA_POLY_EXP_DEFAULT) == _lib.FA_OK  # back to the default
 
 
 def test_masked_validation(lib):

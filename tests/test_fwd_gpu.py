@@ -16,12 +16,12 @@ pytestmark = pytest.mark.gpu
 def _built():
     from exact_attention_94_gb300 import build
     build.build()
-    # the library's defaults: threshold 8, every exponential on the SFU
+    # the library's defaults: threshold 8, one column pair in 16 on the cubic
     ops.set_option(_lib.FA_OPT_RESCALE_TAU, 8.0)
-    ops.set_option(_lib.FA_OPT_POLY_EXP, 0)
+    ops.set_option(_lib.FA_OPT_POLY_EXP, _lib.FA_POLY_EXP_DEFAULT)
     yield
     ops.set_option(_lib.FA_OPT_RESCALE_TAU, 8.0)
-    ops.set_option(_lib.FA_OPT_POLY_EXP, 0)
+    ops.set_option(_lib.FA_OPT_POLY_EXP, _lib.FA_POLY_EXP_DEFAULT)
 
 
 def run_dense(B, H, N, d, causal, seed=0, k_boost=1.0):
@@ -75,7 +75,7 @@ def test_rescale_threshold_and_exp_split(tau, poly, d, causal):
         check_dense(1, 4, 1024 + 33, d, causal, seed=3, k_boost=3.0)
     finally:
         ops.set_option(_lib.FA_OPT_RESCALE_TAU, 8.0)
-        ops.set_option(_lib.FA_OPT_POLY_EXP, 0)
+        ops.set_option(_lib.FA_OPT_POLY_EXP, _lib.FA_POLY_EXP_DEFAULT)
 
 
 def test_large_score_offsets():
