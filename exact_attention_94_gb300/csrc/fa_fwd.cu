@@ -33,6 +33,10 @@
 // The tensor pipe alternates between the two tiles (S0_j, PV1_{j-1}, S1_j,
 // PV0_j, ...) so one tile's softmax overlaps the other tile's products.
 // TMEM columns: S0 [0,128), S1 [128,256), O0 [256,256+d), O1 [256+d,256+2d).
+// d = 128: P overwrites S as bf16 pairs, so a tile's next S waits for its P V.
+// d = 64 (bf16): P has columns of its own, P0 [384,448), P1 [448,512), and a
+// tile's next S is issued as soon as its softmax has read the current S; the
+// order per key tile j is S0_j, S1_j, PV0_{j-1}, PV1_{j-1}.
 #include "fa_internal.h"
 #include "ptx.cuh"
 
@@ -74,6 +78,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using L = FwdLayout<D, F8>;
   constexpr bool MASKED = MASK != kMaskNone;
   constexpr bool LEFT = MASK == kMaskWindow;  // rows' keys may start after key 0
+  constexpr bool SEPP = D == 64 && !F8;       // P in TMEM columns of its own
   constexpr int NS = L::kStages;
   constexpr int CH = (int)(D * L::kElt / 128);  // 128-byte swizzle columns per row
   constexpr int CHUNK_ELEMS = (int)(128 / L::kElt);
@@ -172,8 +177,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // where tile t sees keys), O_EMPTY[t] (tile t's epilogue has read O).  Per
   // visited key tile: S_FULL[t], P_FULL[t], and the K/V ring's FULL/EMPTY
   // slots, whose counts continue from one chunk to the next.
+  // With P in columns of its own (d = 64): S_FREE[t] (the softmax has read
+  // S_t: the next S_t may be issued), P_EMPTY[t] (the P V product has read P_t).
   enum { Q_FULL = 0, Q_EMPTY = 1, KV_FULL = 2, KV_EMPTY = 2 + NS, S_FULL = 2 + 2 * NS, P_FULL = S_FULL + 2,
-         O_FINAL = P_FULL + 2, O_EMPTY = O_FINAL + 2, DRAIN = O_EMPTY + 2, NBARS = DRAIN + 1 };
+         O_FINAL = P_FULL + 2, O_EMPTY = O_FINAL + 2, S_FREE = O_EMPTY + 2, P_EMPTY = S_FREE + 2,
+         DRAIN = P_EMPTY + 2, NBARS = DRAIN + 1 };
   static_assert(8 * NBARS + 8 <= 256, "barrier area");
   const uint32_t bar0 = base + L::kBarOff;
   auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
@@ -192,6 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(BAR(P_FULL + t), 128);
       mbar_init(BAR(O_FINAL + t), 1);
       mbar_init(BAR(O_EMPTY + t), 128);
+      mbar_init(BAR(S_FREE + t), 128);
+      mbar_init(BAR(P_EMPTY + t), 1);
     }
     mbar_init(BAR(DRAIN), 1);
     *abort_flag = 0;
@@ -285,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_PV = [&](int t, int slot, bool acc) {
         const uint32_t va = kv_s + slot * TILE;
         const uint32_t dst = t ? tO1 : tO0;
-        const uint32_t pa = t ? tS1 : tS0;
+        const uint32_t pa = SEPP ? tmem + 384u + 64u * t : (t ? tS1 : tS0);
         if constexpr (F8) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
@@ -300,16 +310,70 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       int ring = 0;                 // K/V ring positions used by earlier chunks
       int sph0 = 0, sph1 = 0;       // S / P phases of each tile used by earlier chunks
-      for (int it = 0; it < n_items && ok; ++it) {
+      // The first P V product of tile t of chunk `it` overwrites O_t: the previous
+      // chunk's epilogue must have read it.
+      auto first_pv_ready = [&](int it, int t) -> bool {
+        if (it == 0) return true;
+        const bool good = __all_sync(0xffffffffu, mbar_wait(BAR(O_EMPTY + t), (it - 1) & 1, w, 10));
+        if (good) tc_fence_after();
+        return good;
+      };
+      if constexpr (SEPP) {
+        // Per key tile j: S0_j, S1_j (each once its softmax has read the tile's
+        // previous S), then PV0_{j-1}, PV1_{j-1} (each once its P has landed).
+        int gs[2] = {0, 0};  // S products issued per tile so far (all chunks)
+        int gp[2] = {0, 0};  // P V products issued per tile so far
+        for (int it = 0; it < n_items && ok; ++it) {
+          int lo[2], hi[2], jmin, jmax;
+          ranges_of(chunk_of(it), lo[0], hi[0], lo[1], hi[1], jmin, jmax);
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(Q_FULL), it & 1, w, 2)))) break;
+          tc_fence_after();
+          for (int j = jmin; j <= jmax && ok; ++j) {
+            if (j < jmax) {
+              const int uk = ring + 2 * (j - jmin), sk = uk % NS;
+              if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(KV_FULL + sk), (uk / NS) & 1, w, 3)))) break;
+              tc_fence_after();
+#pragma unroll
+              for (int t = 0; t < 2; ++t) {
+                if (j < lo[t] || j >= hi[t]) continue;
+                if (gs[t] > 0) {
+                  if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(S_FREE + t), (gs[t] - 1) & 1, w, 11)))) break;
+                  tc_fence_after();
+                }
+                issue_S(t, sk);
+                mma_commit_w(BAR(S_FULL + t));
+                ++gs[t];
+              }
+              if (!ok) break;
+              if (j == jmax - 1) mma_commit_w(BAR(Q_EMPTY));  // the chunk's last S product
+              mma_commit_w(BAR(KV_EMPTY + sk));
+            }
+            if (j > jmin) {
+              const int uv = ring + 2 * (j - 1 - jmin) + 1, sv = uv % NS;
+              if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(KV_FULL + sv), (uv / NS) & 1, w, 5)))) break;
+              tc_fence_after();
+#pragma unroll
+              for (int t = 0; t < 2; ++t) {
+                if (j - 1 < lo[t] || j - 1 >= hi[t]) continue;
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(P_FULL + t), gp[t] & 1, w, 6)))) break;
+                tc_fence_after();
+                if (j - 1 == lo[t] && !(ok = first_pv_ready(it, t))) break;
+                issue_PV(t, sv, j - 1 > lo[t]);
+                mma_commit_w(BAR(P_EMPTY + t));
+                if (j - 1 == hi[t] - 1) mma_commit_w(BAR(O_FINAL + t));
+                ++gp[t];
+              }
+              if (!ok) break;
+              mma_commit_w(BAR(KV_EMPTY + sv));
+            }
+          }
+          if (ok && jmax <= jmin) mma_commit_w(BAR(Q_EMPTY));  // a chunk with no key tile: nothing read Q
+          ring += 2 * (jmax - jmin);
+        }
+      }
+      for (int it = 0; it < n_items && ok && !SEPP; ++it) {
         int jlo0, jhi0, jlo1, jhi1, jmin, jmax;
         ranges_of(chunk_of(it), jlo0, jhi0, jlo1, jhi1, jmin, jmax);
-        // The first P V product of tile t overwrites O_t: the previous chunk's epilogue must have read it.
-        auto first_pv_wait = [&](int t) -> bool {
-          if (it == 0) return true;
-          const bool good = __all_sync(0xffffffffu, mbar_wait(BAR(O_EMPTY + t), (it - 1) & 1, w, 10));
-          if (good) tc_fence_after();
-          return good;
-        };
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(Q_FULL), it & 1, w, 2)))) break;
         tc_fence_after();
         // Ring position u of key tile j is ring + 2 (j - jmin) (K) and + 1 (V);
@@ -328,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(P_FULL + 1), (sph1 + j - 1 - jlo1) & 1, w, 4))))
                 break;
               tc_fence_after();
-              if (j - 1 == jlo1 && !(ok = first_pv_wait(1))) break;
+              if (j - 1 == jlo1 && !(ok = first_pv_ready(it, 1))) break;
               issue_PV(1, sv, j - 1 > jlo1);
               if (j - 1 == jhi1 - 1) mma_commit_w(BAR(O_FINAL + 1));
             }
@@ -348,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(P_FULL + 0), (sph0 + j - jlo0) & 1, w, 6))))
               break;
             tc_fence_after();
-            if (j == jlo0 && !(ok = first_pv_wait(0))) break;
+            if (j == jlo0 && !(ok = first_pv_ready(it, 0))) break;
             issue_PV(0, sv, j > jlo0);
             if (j == jhi0 - 1) mma_commit_w(BAR(O_FINAL + 0));
           }
@@ -359,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j - 1 >= jlo1 && j - 1 < jhi1) {
             if ((ok = __all_sync(0xffffffffu, mbar_wait(BAR(P_FULL + 1), (sph1 + j - 1 - jlo1) & 1, w, 4)))) {
               tc_fence_after();
-              if (j - 1 == jlo1) ok = first_pv_wait(1);
+              if (j - 1 == jlo1) ok = first_pv_ready(it, 1);
               if (ok) {
                 issue_PV(1, sv, j - 1 > jlo1);
                 mma_commit_w(BAR(O_FINAL + 1));
@@ -388,6 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + (t ? 128u : 0u);
     const uint32_t tO = tmem + lane_off + 256u + (t ? (uint32_t)D : 0u);
+    const uint32_t tP = SEPP ? tmem + lane_off + 384u + 64u * (uint32_t)t : tS;  // where P goes
     const float sl2 = p.scale_log2;
     const float tau = p.tau;
 #ifdef FA_COUNT_RESCALES
@@ -452,6 +517,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sr[c]);
         tmem_ld_wait();
+        if constexpr (SEPP) {  // S is in registers: the tile's next S may be issued
+          tc_fence_before();
+          mbar_arrive(BAR(S_FREE + t));
+        }
         float x[128];
   #pragma unroll
         for (int i = 0; i < 128; ++i) x[i] = __uint_as_float(sr[i / 32][i % 32]);
@@ -484,6 +553,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_ref = m_new;
         }
         const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
+        if constexpr (SEPP) {
+          // the previous P V product of this tile must have read P (and be done
+          // adding into O, which a rescale below multiplies)
+          const int g = sphase + j - jlo;
+          if (g > 0) {
+            ok = mbar_wait(BAR(P_EMPTY + t), (g - 1) & 1, w, 12);
+            if (!__all_sync(0xffffffffu, ok)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+        }
 
         // p = 2^(x * scale * log2 e - m_ref): packed FMA, exponentials, packed partial sums
         const uint64_t sl2x2 = f2_pack(sl2j, sl2j);
@@ -510,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               ph0 = p0, ph1 = p1;
           } else {
             pk[i / 32][i % 32] = pack_bf16x2(p0, p1);
-            if (i == 31) tmem_st32(tS, pk[0]);  // first half of P out early: frees registers
+            if (i == 31) tmem_st32(tP, pk[0]);  // first half of P out early: frees registers
           }
         }
         float s0, s1, s2, s3, s4, s5, s6, s7;
@@ -535,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (F8)
           tmem_st32(tS, pk[0]);  // the whole tile's P: 32 columns of four e4m3 each
         else
-          tmem_st32(tS + 32, pk[1]);
+          tmem_st32(tP + 32, pk[1]);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(BAR(P_FULL + t));
