@@ -419,10 +419,36 @@ def run_e2e(args, ctx):
     flops = F * (2.5 if have_bwd else 1.0)
     h2d = sum(t.numel() * t.element_size() for t in host_in[0].values())
     d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
+    link = link_bandwidth(torch)
+    # with the copies overlapped, a step can go no faster than its slower copy direction
+    copy_ms = max(h2d / link["h2d_gbs"], d2h / link["d2h_gbs"]) * 1e-6
     return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "timing": "CUDA events joined across the three streams",
-            "pipelining": "3 streams, double-buffered device tensors"}
+            "pipelining": "3 streams, double-buffered device tensors",
+            "link": {**link, "copy_ms_per_step": round(copy_ms, 4),
+                     "copy_bound_tflops": round(flops / (copy_ms * 1e-3) / 1e12, 2)}}
+
+
+def link_bandwidth(torch, nbytes=256 << 20, reps=5):
+    """Host<->device copy rates between pinned host memory and the GPU, one
+    direction at a time (CUDA events), for judging the e2e figure."""
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    out = {}
+    for name, fn in (("h2d_gbs", lambda: d.copy_(h, non_blocking=True)),
+                     ("d2h_gbs", lambda: h.copy_(d, non_blocking=True))):
+        fn()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(reps):
+            fn()
+        e.record()
+        torch.cuda.synchronize()
+        out[name] = round(nbytes * reps / (s.elapsed_time(e) * 1e-3) / 1e9, 1)
+    del h, d
+    return out
 
 
 def time_calls(torch, fn, warm=2, iters=5):
