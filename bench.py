@@ -420,8 +420,9 @@ def run_e2e(args, ctx):
     h2d = sum(t.numel() * t.element_size() for t in host_in[0].values())
     d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
     link = link_bandwidth(torch)
-    # with the copies overlapped, a step can go no faster than its slower copy direction
-    copy_ms = max(h2d / link["h2d_gbs"], d2h / link["d2h_gbs"]) * 1e-6
+    # with the copies overlapped with compute and with each other, a step can go no faster
+    # than its slower copy direction alone, nor than both directions' bytes at the joint rate
+    copy_ms = max(h2d / link["h2d_gbs"], d2h / link["d2h_gbs"], (h2d + d2h) / link["both_directions_gbs"]) * 1e-6
     return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "timing": "CUDA events joined across the three streams",
@@ -431,23 +432,43 @@ def run_e2e(args, ctx):
 
 
 def link_bandwidth(torch, nbytes=256 << 20, reps=5):
-    """Host<->device copy rates between pinned host memory and the GPU, one
-    direction at a time (CUDA events), for judging the e2e figure."""
-    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
-    d = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    """Host<->device copy rates between pinned host memory and the GPU (CUDA
+    events), for judging the e2e figure: each direction alone, and both at
+    once on two streams (what the pipelined e2e leg does), as total bytes
+    over the joint time."""
+    h_in = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    h_out = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d_in = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    d_out = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    s_a, s_b = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def both():
+        with torch.cuda.stream(s_a):
+            d_in.copy_(h_in, non_blocking=True)
+        with torch.cuda.stream(s_b):
+            h_out.copy_(d_out, non_blocking=True)
+
     out = {}
-    for name, fn in (("h2d_gbs", lambda: d.copy_(h, non_blocking=True)),
-                     ("d2h_gbs", lambda: h.copy_(d, non_blocking=True))):
+    for name, fn, nb in (("h2d_gbs", lambda: d_in.copy_(h_in, non_blocking=True), nbytes),
+                         ("d2h_gbs", lambda: h_out.copy_(d_out, non_blocking=True), nbytes),
+                         ("both_directions_gbs", both, 2 * nbytes)):
         fn()
         torch.cuda.synchronize()
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s.record()
+        cur = torch.cuda.current_stream()
+        s.record(cur)
+        for st in (s_a, s_b):
+            st.wait_event(s)
         for _ in range(reps):
             fn()
-        e.record()
+        for st in (s_a, s_b):
+            ev = torch.cuda.Event()
+            ev.record(st)
+            cur.wait_event(ev)
+        e.record(cur)
         torch.cuda.synchronize()
-        out[name] = round(nbytes * reps / (s.elapsed_time(e) * 1e-3) / 1e9, 1)
-    del h, d
+        out[name] = round(nb * reps / (s.elapsed_time(e) * 1e-3) / 1e9, 1)
+    del h_in, h_out, d_in, d_out
     return out
 
 
