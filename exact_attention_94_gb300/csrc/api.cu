@@ -221,9 +221,14 @@ static int packed_items(int num_seqs, int units_max, int total_rows, int unit) {
   return (int)items;
 }
 
-// The sliding-window and e4m3 kernels exist with the cubic off or on one
-// column pair in 8: a share of 1/16 maps to off, 1/4 and 1/8 to 1/8.
+// The sliding-window kernels exist with the cubic off or on one column pair
+// in 8: a share of 1/16 maps to off, 1/4 and 1/8 to 1/8.  The e4m3 kernels
+// without a window also have 1/16 (the fastest share measured for them).
 static int window_poly(int poly) { return (poly == 4 || poly == 8) ? 8 : 0; }
+static int fp8_poly(int poly, int mask) {
+  if (mask == kMaskWindow) return window_poly(poly);
+  return poly == 16 ? 16 : window_poly(poly);
+}
 
 static fa_status fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu,
                             const int* cu_k, int nbatch, int n_rows, int n_rows_k, int seq_len, int seq_len_k,
@@ -568,7 +573,7 @@ fa_status fa_fwd_fp8(const void* q_codes, const void* k_codes, const void* vt_co
   p.tau = g_opt.tau;
   p.err = g_err_ptr;
   p.timeout_ns = g_opt.timeout_ns;
-  cudaError_t e = launch_fwd_fp8(tq, tk, tvt, p, mask_kind(wl, wr), window_poly(g_opt.poly), B * Hq,
+  cudaError_t e = launch_fwd_fp8(tq, tk, tvt, p, mask_kind(wl, wr), fp8_poly(g_opt.poly, mask_kind(wl, wr)), B * Hq,
                                  (cudaStream_t)stream);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }

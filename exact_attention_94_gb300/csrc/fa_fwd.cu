@@ -727,8 +727,10 @@ cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const C
   if (mask == MM && poly == PP) return launch_fwd_t<128, MM, PP, true>(tq, tk, tvt, p, grid_x, stream);
   FA_FP8_CASE(kMaskNone, 0)
   FA_FP8_CASE(kMaskNone, 8)
+  FA_FP8_CASE(kMaskNone, 16)
   FA_FP8_CASE(kMaskRight, 0)
   FA_FP8_CASE(kMaskRight, 8)
+  FA_FP8_CASE(kMaskRight, 16)
   FA_FP8_CASE(kMaskWindow, 0)
   FA_FP8_CASE(kMaskWindow, 8)
 #undef FA_FP8_CASE

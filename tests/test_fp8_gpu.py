@@ -151,6 +151,19 @@ def test_fp8_forward_rescale_threshold(tau):
         ops.set_option(_lib.FA_OPT_RESCALE_TAU, 8.0)
 
 
+@pytest.mark.parametrize("poly", [0, 4, 8, 16])
+def test_fp8_forward_cubic_share(poly):
+    """The e4m3 kernels with none, 1/8 or 1/16 of the exponentials' column
+    pairs on the FMA-pipe cubic (4 selects 1/8) give the same attention."""
+    ops.set_option(_lib.FA_OPT_POLY_EXP, poly)
+    try:
+        test_fp8_forward_statistical((2, 300, 300, 4, 2, -1, 0, True))
+        test_fp8_forward_statistical((1, 512, 512, 2, 2, -1, 0, False))
+        test_fp8_forward_statistical((1, 640, 640, 2, 2, 100, 0, True))
+    finally:
+        ops.set_option(_lib.FA_OPT_POLY_EXP, _lib.FA_POLY_EXP_DEFAULT)
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_fp8_forward_exact_when_p_is_representable(causal):
     """Q = 0 makes every score 0, so P = 1 before normalisation; V blocks that
