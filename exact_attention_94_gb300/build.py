@@ -98,5 +98,41 @@ def build_counting(verbose: bool = False) -> str:
     return COUNT_LIB
 
 
+BOUNDS_LIB = os.path.join(HERE, "libfa_bounds.so")
+BOUNDS_SOURCES = ("fa_fwd.cu", "fa_bwd.cu", "fa_decode.cu")
+
+
+def build_bounds(verbose: bool = False) -> str:
+    """A test-only variant of the library: the forward, backward and decode
+    kernels compiled with FA_BOUNDS_CHECK, so that every plain (non-TMA)
+    global load, store and atomic they make checks its index against its
+    buffer and records an error code instead of touching memory outside it.
+    Linked from the product's other objects; the product libfa.so has no
+    checks."""
+    build(verbose=verbose)
+    nvcc = _nvcc()
+
+    def run(cmd):
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + r.stdout + r.stderr)
+
+    objs, jobs = [], []
+    for n in SOURCES:
+        if n in BOUNDS_SOURCES:
+            src = os.path.join(CSRC, n)
+            obj = os.path.join(BUILD, os.path.splitext(n)[0] + "_bounds.o")
+            if _stale(obj, _deps(src)):
+                jobs.append([nvcc, *ARCH, *FLAGS, "-DFA_BOUNDS_CHECK", "-c", src, "-o", obj])
+            objs.append(obj)
+        else:
+            objs.append(os.path.join(BUILD, os.path.splitext(n)[0] + ".o"))
+    with ThreadPoolExecutor(max_workers=max(1, len(jobs))) as ex:
+        list(ex.map(run, jobs))
+    if _stale(BOUNDS_LIB, objs):
+        run([nvcc, *ARCH, "-shared", "-o", BOUNDS_LIB, *objs])
+    return BOUNDS_LIB
+
+
 if __name__ == "__main__":
     print(build(verbose=True))

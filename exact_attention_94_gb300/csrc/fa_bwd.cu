@@ -223,6 +223,8 @@ __device__ void bwd_zero_dkdv(const BwdParams& p, const BwdItem& it, int Hkv, in
   for (int idx = (int)threadIdx.x; idx < nk * (D / 8); idx += (int)blockDim.x) {
     const int r = idx / (D / 8), c = idx % (D / 8);
     const size_t grow = ((size_t)it.b_coord * p.n_rows_k + it.kv_start + k0 + r) * Hkv + h_kv;
+    if (!FA_INB(grow * D + c * 8, grow * D + c * 8 + 7, (long long)p.B_tensor * p.n_rows_k * Hkv * D, p.err, 17))
+      continue;
     reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dk) + grow * D)[c] = make_uint4(0u, 0u, 0u, 0u);
     reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dv) + grow * D)[c] = make_uint4(0u, 0u, 0u, 0u);
   }
@@ -550,7 +552,8 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
     bool f_ok = false;
     auto fetch = [&]() {
       const int qg = q_begin + f_blk * 128 + 64 * g + (kr & 63);
-      f_ok = f_hq < hq_end && qg < seq_len;
+      f_ok = f_hq < hq_end && qg < seq_len &&
+             FA_INB(row_base_of(f_hq) + qg, row_base_of(f_hq) + qg, (long long)p.B_tensor * p.H * p.n_rows, p.err, 13);
       f_raw = f_ok ? fsrc[row_base_of(f_hq) + qg] : 0.f;
       if (++f_blk == n_q) {
         f_blk = 0;
@@ -674,6 +677,8 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
       if (__all_sync(0xffffffffu, ok)) {
         tc_fence_after();
         const size_t grow = ((size_t)b_coord * p.n_rows_k + kv_start + kg) * Hkv + h_kv;
+        const bool store_ok =
+            row_ok && FA_INB(grow * D, grow * D + D - 1, (long long)p.B_tensor * p.n_rows_k * Hkv * D, p.err, 16);
         const uint32_t src = tmem + lane_off + 256u + (g ? (uint32_t)D : 0u);
         __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(g ? p.dk : p.dv) + grow * D;
 #pragma unroll
@@ -684,7 +689,7 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-          if (row_ok) {
+          if (store_ok) {
             uint4* o4 = reinterpret_cast<uint4*>(dst + 32 * c);
 #pragma unroll
             for (int i = 0; i < 4; ++i) o4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
@@ -711,7 +716,11 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(BAR(DQ_EMPTY));  // the columns are free for the next dQ
-      if (qg < it.q_hi) {  // rows past q_hi see none of this block's keys: their share is zero
+      const long long acc_base = (long long)(b_coord * p.H + hq_of(n)) * (D / 4) * p.n_rows;
+      const long long n_acc4 = (long long)p.B_tensor * p.H * (D / 4) * p.n_rows;
+      if (qg < it.q_hi &&  // rows past q_hi see none of this block's keys: their share is zero
+          FA_INB(acc_base + (size_t)(8 * half) * p.n_rows + seq_start + qg,
+                 acc_base + (size_t)(8 * half + 7) * p.n_rows + seq_start + qg, n_acc4, p.err, 14)) {
         const size_t row = (size_t)seq_start + qg;
 #pragma unroll
         for (int j = 0; j < 8; ++j)
@@ -731,7 +740,11 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
     for (int n = 0; n < n_steps; ++n) {
       float* acc = p.dq_acc + row_base_of(hq_of(n)) * D + dr;  // [B*H][rows][d]: a warp's lanes cover 128 bytes
       const int q0 = q_begin + (n % n_q) * 128 + 64 * half;
-      const int nq = min(64, it.q_hi - q0);  // rows past q_hi see none of this block's keys
+      int nq = min(64, it.q_hi - q0);  // rows past q_hi see none of this block's keys
+      const long long acc_first = (long long)row_base_of(hq_of(n)) * D + dr + (long long)q0 * D;
+      if (nq > 0 && !FA_INB(acc_first, acc_first + (long long)(nq - 1) * D, (long long)p.B_tensor * p.H * p.n_rows * D,
+                            p.err, 15))
+        nq = 0;
       bool ok = mbar_wait(BAR(DQ_FULL), n & 1, w, 60);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();

@@ -116,7 +116,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) fa_decode_split_kernel(const D
       // table is read once per page, when the walk enters it
       int pblk = 0, pslot = 0, page = 0;
       auto lookup = [&]() {
-        page = p.block_table[(size_t)b * p.max_blocks + pblk];
+        const size_t ti = (size_t)b * p.max_blocks + pblk;
+        page = FA_INB(ti, ti, (long long)p.B * p.max_blocks, p.err, 20) ? p.block_table[ti] : 0;
         if (page < 0 || page >= p.num_pages) {  // report, and read a valid page instead
           atomicCAS(p.err, 0u, FA_DEVERR_BAD_PAGE);
           page = 0;
@@ -146,6 +147,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) fa_decode_split_kernel(const D
           } else {
             row = ((size_t)b * p.L + l) * p.Hkv * D + kv_head0;
           }
+          // (bounds-checked builds: a row outside the cache is reported and the group's row 0 read instead,
+          // so that the stage's byte count still completes)
+          if (!FA_INB(row, row + (size_t)G * D - 1,
+                      p.block_table != nullptr ? (long long)p.num_pages * p.page_size * p.Hkv * D
+                                               : (long long)p.B * p.L * p.Hkv * D,
+                      p.err, 21))
+            row = kv_head0;
           bulk_load(dk + m * row_bytes, static_cast<const __nv_bfloat16*>(p.k) + row, row_bytes, FULL(slot));
           bulk_load(dk + (kDecT + m) * row_bytes, static_cast<const __nv_bfloat16*>(p.v) + row, row_bytes,
                     FULL(slot));
@@ -169,9 +177,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) fa_decode_split_kernel(const D
       l_lane[j] = 0.f;
 #pragma unroll
       for (int e = 0; e < E; ++e) o[j][e] = 0.f;
-      if (hj < Gq) {
-        const __nv_bfloat16* qs =
-            static_cast<const __nv_bfloat16*>(p.q) + ((size_t)b * p.H + hg * Gq + hj) * D + lane * E;
+      const size_t q_off = ((size_t)b * p.H + hg * Gq + hj) * D + lane * E;
+      if (hj < Gq && FA_INB(q_off, q_off + E - 1, (long long)p.B * p.H * D, p.err, 22)) {
+        const __nv_bfloat16* qs = static_cast<const __nv_bfloat16*>(p.q) + q_off;
         load_row<E>(qs, qv[j]);
 #pragma unroll
         for (int e = 0; e < E; ++e) qv[j][e] *= p.scale_log2;  // scores come out in log2 units
@@ -247,6 +255,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) fa_decode_split_kernel(const D
         float l = l_lane[j] + __shfl_xor_sync(0xffffffffu, l_lane[j], 8);
         l += __shfl_xor_sync(0xffffffffu, l, 16);
         const size_t pidx = ((size_t)b * p.H + hg * Gq + hj) * p.num_splits + c;
+        if (!FA_INB(pidx, pidx, (long long)p.B * p.H * p.num_splits, p.err, 23)) continue;
         const float inv = l > 0.f ? 1.f / l : 0.f;
         float* dst = p.part_o + pidx * D + lane * E;
 #pragma unroll

@@ -126,6 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int h_kv = h / p.kv_group;  // grouped-query attention: K/V head shared by kv_group query heads
   int seq_start = 0, seq_len = p.seq_len, kv_start = 0, kv_len = p.seq_len_k, b_coord = b;
   if (p.cu_seqlens != nullptr) {
+    if (!FA_INB(b, b + 1, p.bh_total / p.H + 1, p.err, 1)) return;  // uniform for the CTA
     seq_start = p.cu_seqlens[b];
     seq_len = p.cu_seqlens[b + 1] - seq_start;
     kv_start = p.cu_seqlens_k[b];
@@ -467,12 +468,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     float sv_ref = 1.f;
     const float* k_sc = nullptr;
     const float* v_sc = nullptr;
+    const long long n_kv_scales = (long long)(p.bh_total / p.H) * (p.H / p.kv_group) * p.n_kblk;
+    const long long hk = (long long)b * (p.H / p.kv_group) + h_kv;
     if constexpr (F8) {
-      const size_t hk = (size_t)b * (p.H / p.kv_group) + h_kv;
       k_sc = p.k_scale + hk * p.n_kblk;
       v_sc = p.v_scale + hk * p.n_kblk;
       float mv = 0.f;
-      for (int i = lane; i < p.n_kblk; i += 32) mv = fmaxf(mv, v_sc[i]);
+      for (int i = lane; i < p.n_kblk; i += 32)
+        if (FA_INB(hk * p.n_kblk + i, hk * p.n_kblk + i, n_kv_scales, p.err, 5)) mv = fmaxf(mv, v_sc[i]);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, o));
       sv_ref = mv > 0.f ? mv : 1.f;
@@ -493,7 +496,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       float sl2_q = sl2;
       if constexpr (F8) {
         const int qb = (q0 >> 7) + t;  // past the last block only when this tile has no rows
-        sl2_q = qb < p.n_qblk ? sl2 * p.q_scale[((size_t)b * p.H + h) * p.n_qblk + qb] : 0.f;
+        const size_t qsi = ((size_t)b * p.H + h) * p.n_qblk + qb;
+        sl2_q = (qb < p.n_qblk && FA_INB(qsi, qsi, (long long)p.bh_total * p.n_qblk, p.err, 6)) ? sl2 * p.q_scale[qsi]
+                                                                                               : 0.f;
       }
 
       for (int j = jlo; j < jhi; ++j) {
@@ -502,8 +507,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // an all-zero Q or K block (scale 0) has all-zero codes, so its scores are
           // exactly 0 under any positive multiplier; a positive one keeps masked
           // -inf scores at -inf instead of turning them into NaN
-          sl2j = fmaxf(sl2_q * k_sc[j], 1e-30f);
-          const float rv = fmaxf(v_sc[j] / sv_ref, 0x1p-30f);  // a zero block's P rounds to 0 either way
+          const bool sc_ok = FA_INB(hk * p.n_kblk + j, hk * p.n_kblk + j, n_kv_scales, p.err, 7);
+          sl2j = fmaxf(sl2_q * (sc_ok ? k_sc[j] : 0.f), 1e-30f);
+          const float rv = fmaxf((sc_ok ? v_sc[j] : 0.f) / sv_ref, 0x1p-30f);  // a zero block's P rounds to 0 either way
           lrv = log2f(rv);
           inv_rv = 1.f / rv;
         }
@@ -625,10 +631,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       sphase += jhi - jlo;
       if (!ok) break;
       // ---------------------------------------------------------- epilogue of the chunk
-      const bool row_ok = row < seq_len;
-      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) +
-                            (((size_t)b_coord * p.n_rows + seq_start + row) * p.H + h) * D;
-      float* lse_out = p.lse + ((size_t)b_coord * p.H + h) * p.n_rows + seq_start + row;
+      const long long o_off = (((long long)b_coord * p.n_rows + seq_start + row) * p.H + h) * D;
+      const long long l_off = ((long long)b_coord * p.H + h) * p.n_rows + seq_start + row;
+      const long long b_tensor = p.cu_seqlens != nullptr ? 1 : p.bh_total / p.H;
+      const bool row_ok = row < seq_len &&
+                          FA_INB(o_off, o_off + D - 1, b_tensor * p.n_rows * p.H * D, p.err, 2) &&
+                          FA_INB(l_off, l_off, b_tensor * p.H * p.n_rows, p.err, 3);
+      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + o_off;
+      float* lse_out = p.lse + l_off;
       if (jhi <= jlo) {
         // no key tile visible to any row of this tile: O = 0, lse = -inf
         if (row_ok) {

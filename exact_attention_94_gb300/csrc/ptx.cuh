@@ -15,7 +15,27 @@ enum : unsigned {
   FA_DEVERR_TIMEOUT_BASE = 0x1000u,  // + site id
   FA_DEVERR_BAD_PAGE = 0x2000u,      // a block-table entry outside the page pool
   FA_DEVERR_BAD_SEQLEN = 0x2001u,    // a sequence length outside [0, max_seq_len]
+  FA_DEVERR_BOUNDS_BASE = 0x3000u,   // + site id: an index outside its buffer (bounds-checked builds only)
 };
+
+// Bounds checks of the plain (non-TMA) global loads, stores and atomics.  In
+// a build with FA_BOUNDS_CHECK defined (a test build; never the product
+// library) FA_INB(first, last, n, err, site) is true when elements first ..
+// last of an n-element buffer are all inside it; otherwise it records
+// FA_DEVERR_BOUNDS_BASE + site in the device error word and is false, and
+// the caller skips the access.  In every other build it is the constant true.
+#ifdef FA_BOUNDS_CHECK
+__device__ __forceinline__ bool fa_in_bounds(long long first, long long last, long long n, unsigned* err,
+                                             unsigned site) {
+  if (first >= 0 && last >= first && last < n) return true;
+  if (err != nullptr) atomicCAS(err, 0u, FA_DEVERR_BOUNDS_BASE + site);
+  return false;
+}
+#define FA_INB(first, last, n, err, site) \
+  ::fa::fa_in_bounds((long long)(first), (long long)(last), (long long)(n), (err), (site))
+#else
+#define FA_INB(first, last, n, err, site) true
+#endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
