@@ -690,9 +690,14 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
           if (store_ok) {
-            uint4* o4 = reinterpret_cast<uint4*>(dst + 32 * c);
+            if ((reinterpret_cast<uintptr_t>(dst) & 31) == 0) {  // whole 32-byte sectors per store
+              st_global_v8(dst + 32 * c, pk);
+              st_global_v8(dst + 32 * c + 16, pk + 8);
+            } else {
+              uint4* o4 = reinterpret_cast<uint4*>(dst + 32 * c);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) o4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+              for (int i = 0; i < 4; ++i) o4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
           }
         }
       }

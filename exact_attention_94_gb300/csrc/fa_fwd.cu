@@ -666,9 +666,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 16; ++i)
             pkd[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
           if (row_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+            if ((reinterpret_cast<uintptr_t>(orow) & 31) == 0) {  // whole 32-byte sectors per store
+              st_global_v8(orow + 32 * c, pkd);
+              st_global_v8(orow + 32 * c + 16, pkd + 8);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
+              for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
+            }
           }
         }
         if (row_ok) *lse_out = l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;

@@ -25,19 +25,21 @@ GUARD = 4096  # bytes before and after each view (a multiple of 16: views stay 1
 
 
 class Guarded:
-    """A tensor of `shape` and `dtype` carved out of a sentinel-filled buffer."""
+    """A tensor of `shape` and `dtype` carved out of a sentinel-filled buffer,
+    `shift` bytes past the guard band (a multiple of 16)."""
 
-    def __init__(self, shape, dtype):
+    def __init__(self, shape, dtype, shift=0):
         n = int(np.prod(shape)) * torch.tensor([], dtype=dtype).element_size()
         self.nbytes = n
-        self.buf = torch.full((GUARD + n + GUARD,), SENTINEL, dtype=torch.uint8, device="cuda")
-        self.t = self.buf[GUARD:GUARD + n].view(dtype).view(shape) if n else torch.empty(shape, dtype=dtype,
-                                                                                            device="cuda")
+        self.lo = GUARD + shift
+        self.buf = torch.full((self.lo + n + GUARD,), SENTINEL, dtype=torch.uint8, device="cuda")
+        self.t = self.buf[self.lo:self.lo + n].view(dtype).view(shape) if n else torch.empty(shape, dtype=dtype,
+                                                                                              device="cuda")
 
     def check(self, what):
         torch.cuda.synchronize()
-        head = self.buf[:GUARD]
-        tail = self.buf[GUARD + self.nbytes:]
+        head = self.buf[:self.lo]
+        tail = self.buf[self.lo + self.nbytes:]
         bad_h = int((head != SENTINEL).sum())
         bad_t = int((tail != SENTINEL).sum())
         assert bad_h == 0 and bad_t == 0, f"{what}: {bad_h} bytes before and {bad_t} after the buffer changed"
@@ -84,6 +86,35 @@ def test_dense_forward_backward_stay_in_bounds(d, causal, N):
         gg.check(name)
         assert torch.allclose(gg.t.float(), r.float(), rtol=2e-2, atol=1e-3), name
     ws.check("workspace")
+    assert ops.device_error() == 0
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_outputs_16_but_not_32_byte_aligned(d):
+    """Rows of O, dK and dV are written 32 bytes per store when their address
+    allows it and 16 bytes per store otherwise: outputs placed 16 bytes off a
+    32-byte boundary take the second path, with the same results and nothing
+    written outside."""
+    B, H, N = 2, 3, 257
+    x = synth.make_dense(B, H, N, d, seed=77, device="cuda")
+    q, k, v, do = x["q"], x["k"], x["v"], x["do"]
+    o_ref, l_ref = ops.fwd(q, k, v, causal=True)
+    o, lse = Guarded(q.shape, torch.bfloat16, shift=16), Guarded((B, H, N), torch.float32, shift=16)
+    assert o.t.data_ptr() % 32 == 16
+    ops.fwd(q, k, v, causal=True, out=o.t, lse=lse.t)
+    o.check("O")
+    lse.check("lse")
+    _same(o.t, o_ref, "O")
+    _bitwise_or_both_nan(lse.t, l_ref, "lse")
+    ref = ops.bwd(q, k, v, o_ref, l_ref, do, causal=True)
+    g = [Guarded(q.shape, torch.bfloat16, shift=16) for _ in range(3)]
+    ops.bwd(q, k, v, o_ref, l_ref, do, causal=True, out=tuple(t.t for t in g))
+    for name, gg, r in zip(("dq", "dk", "dv"), g, ref):
+        gg.check(name)
+        if name == "dq":
+            assert torch.allclose(gg.t.float(), r.float(), rtol=2e-2, atol=1e-3), name
+        else:
+            _same(gg.t, r, name)
     assert ops.device_error() == 0
 
 
