@@ -122,41 +122,65 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16* __
   }
 }
 
-// dq[bt][n][h][c] = bf16(dQ accumulator), 8 columns per thread.
+// dq[bt][n][h][c] = bf16(dQ accumulator).
+//   d = 128: 8 columns per thread; a row's 16 threads read 512 contiguous
+//            accumulator bytes and write the row's 256 bytes.
+//   d = 64 : 16 columns per thread; the 32 threads of a warp take 32
+//            consecutive rows of one 16-column group (four planes of the
+//            [B*H][d/4][rows][4] layout, 512 contiguous bytes each) and write
+//            32 bytes (one L2 sector) of their row each.
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_post_kernel(const float* __restrict__ dq_acc,
                                                          __nv_bfloat16* __restrict__ dq, int H, int n_rows) {
-  constexpr int TPR = D / 8;
-  constexpr int RPP = 256 / TPR;
-  constexpr int PASSES = kRowTile / RPP;
   long long bh;
   int n0;
   row_tile_of(H, n_rows, bh, n0);
   const long long bt = bh / H;
   const int h = (int)(bh - bt * H);
-  // d = 128: a row's 16 threads read 512 contiguous accumulator bytes; d = 64: the
-  // threads of a warp take 32 consecutive rows of one column pair (512 contiguous bytes
-  // per plane of the [B*H][d/4][rows][4] layout)
-  const int c8 = D == 128 ? (int)threadIdx.x % TPR : (int)threadIdx.x / RPP;
-  const int rl = D == 128 ? (int)threadIdx.x / TPR : (int)threadIdx.x % RPP;
   const float4* acc4 = reinterpret_cast<const float4*>(dq_acc);
-  float4 v0[PASSES], v1[PASSES];
+  if constexpr (D == 128) {
+    constexpr int TPR = D / 8;
+    constexpr int RPP = 256 / TPR;
+    constexpr int PASSES = kRowTile / RPP;
+    const int c8 = (int)threadIdx.x % TPR, rl = (int)threadIdx.x / TPR;
+    float4 v0[PASSES], v1[PASSES];
 #pragma unroll
-  for (int k = 0; k < PASSES; ++k) {
-    const int n = n0 + rl + k * RPP;
-    v0[k] = v1[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (n < n_rows) {
-      v0[k] = acc4[acc_f4_index<D>((size_t)bh, n_rows, n, 2 * c8)];
-      v1[k] = acc4[acc_f4_index<D>((size_t)bh, n_rows, n, 2 * c8 + 1)];
+    for (int k = 0; k < PASSES; ++k) {
+      const int n = n0 + rl + k * RPP;
+      v0[k] = v1[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (n < n_rows) {
+        v0[k] = acc4[acc_f4_index<D>((size_t)bh, n_rows, n, 2 * c8)];
+        v1[k] = acc4[acc_f4_index<D>((size_t)bh, n_rows, n, 2 * c8 + 1)];
+      }
     }
-  }
 #pragma unroll
-  for (int k = 0; k < PASSES; ++k) {
-    const int n = n0 + rl + k * RPP;
+    for (int k = 0; k < PASSES; ++k) {
+      const int n = n0 + rl + k * RPP;
+      if (n < n_rows) {
+        const uint4 out = make_uint4(pack_bf16x2(v0[k].x, v0[k].y), pack_bf16x2(v0[k].z, v0[k].w),
+                                     pack_bf16x2(v1[k].x, v1[k].y), pack_bf16x2(v1[k].z, v1[k].w));
+        *reinterpret_cast<uint4*>(dq + (((size_t)bt * n_rows + n) * H + h) * D + c8 * 8) = out;
+      }
+    }
+  } else {
+    const int warp = (int)threadIdx.x >> 5;
+    const int c16 = warp & 3;                                  // columns 16 * c16 .. + 15
+    const int n = n0 + (warp >> 2) * 32 + (int)(threadIdx.x & 31);  // 8 warps: 4 groups x 2 x 32 rows
     if (n < n_rows) {
-      const uint4 out = make_uint4(pack_bf16x2(v0[k].x, v0[k].y), pack_bf16x2(v0[k].z, v0[k].w),
-                                   pack_bf16x2(v1[k].x, v1[k].y), pack_bf16x2(v1[k].z, v1[k].w));
-      *reinterpret_cast<uint4*>(dq + (((size_t)bt * n_rows + n) * H + h) * D + c8 * 8) = out;
+      uint32_t pk[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 a = acc4[acc_f4_index<D>((size_t)bh, n_rows, n, 4 * c16 + j)];
+        pk[2 * j] = pack_bf16x2(a.x, a.y);
+        pk[2 * j + 1] = pack_bf16x2(a.z, a.w);
+      }
+      __nv_bfloat16* dst = dq + (((size_t)bt * n_rows + n) * H + h) * D + c16 * 16;
+      if ((reinterpret_cast<uintptr_t>(dst) & 31) == 0) {
+        st_global_v8(dst, pk);
+      } else {
+        reinterpret_cast<uint4*>(dst)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        reinterpret_cast<uint4*>(dst)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      }
     }
   }
 }
@@ -721,11 +745,11 @@ __global__ void __launch_bounds__(kBwd128Threads, 1)
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(BAR(DQ_EMPTY));  // the columns are free for the next dQ
-      const long long acc_base = (long long)(b_coord * p.H + hq_of(n)) * (D / 4) * p.n_rows;
-      const long long n_acc4 = (long long)p.B_tensor * p.H * (D / 4) * p.n_rows;
+      [[maybe_unused]] const long long acc_base = (long long)(b_coord * p.H + hq_of(n)) * (D / 4) * p.n_rows;
       if (qg < it.q_hi &&  // rows past q_hi see none of this block's keys: their share is zero
           FA_INB(acc_base + (size_t)(8 * half) * p.n_rows + seq_start + qg,
-                 acc_base + (size_t)(8 * half + 7) * p.n_rows + seq_start + qg, n_acc4, p.err, 14)) {
+                 acc_base + (size_t)(8 * half + 7) * p.n_rows + seq_start + qg,
+                 (long long)p.B_tensor * p.H * (D / 4) * p.n_rows, p.err, 14)) {
         const size_t row = (size_t)seq_start + qg;
 #pragma unroll
         for (int j = 0; j < 8; ++j)

@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float sv_ref = 1.f;
     const float* k_sc = nullptr;
     const float* v_sc = nullptr;
-    const long long n_kv_scales = (long long)(p.bh_total / p.H) * (p.H / p.kv_group) * p.n_kblk;
+    [[maybe_unused]] const long long n_kv_scales = (long long)(p.bh_total / p.H) * (p.H / p.kv_group) * p.n_kblk;
     const long long hk = (long long)b * (p.H / p.kv_group) + h_kv;
     if constexpr (F8) {
       k_sc = p.k_scale + hk * p.n_kblk;
@@ -633,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------------- epilogue of the chunk
       const long long o_off = (((long long)b_coord * p.n_rows + seq_start + row) * p.H + h) * D;
       const long long l_off = ((long long)b_coord * p.H + h) * p.n_rows + seq_start + row;
-      const long long b_tensor = p.cu_seqlens != nullptr ? 1 : p.bh_total / p.H;
+      [[maybe_unused]] const long long b_tensor = p.cu_seqlens != nullptr ? 1 : p.bh_total / p.H;
       const bool row_ok = row < seq_len &&
                           FA_INB(o_off, o_off + D - 1, b_tensor * p.n_rows * p.H * D, p.err, 2) &&
                           FA_INB(l_off, l_off, b_tensor * p.H * p.n_rows, p.err, 3);
