@@ -570,8 +570,8 @@ def run_extra(peaks):
     qc, qs = ops.fp8_quantize(x["q"], signs)
     kc, ks = ops.fp8_quantize(x["k"], signs)
     vc, vs = ops.fp8_quantize(x["v"], None, transpose=True)
-    t_att = time_calls(torch, lambda: ops.fwd_fp8_codes(qc, kc, vc, qs, ks, vs, causal=True), iters=10)
-    t_all = time_calls(torch, lambda: ops.fwd_fp8(x["q"], x["k"], x["v"], signs, causal=True), iters=10)
+    t_att = time_calls(torch, lambda: ops.fwd_fp8_codes(qc, kc, vc, qs, ks, vs, causal=True), warm=3, iters=20)
+    t_all = time_calls(torch, lambda: ops.fwd_fp8(x["q"], x["k"], x["v"], signs, causal=True), warm=3, iters=20)
     fp8_peak = 2.0 * peaks["bf16_tflops"]  # measured bf16 burst x the nominal e4m3 / bf16 ratio of 2
     out["fp8"] = {"attn_ms": round(t_att, 4), "attn_tflops": round(F / t_att / 1e9, 1),
                   "attn_frac_of_fp8_peak": round(F / t_att / 1e9 / fp8_peak, 4),
