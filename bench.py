@@ -488,7 +488,7 @@ def link_bandwidth(torch, nbytes=256 << 20, reps=5, trials=3):
     return out
 
 
-def time_calls(torch, fn, warm=2, iters=5):
+def time_calls(torch, fn, warm=3, iters=10):
     for _ in range(warm):
         fn()
     torch.cuda.synchronize()
