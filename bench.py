@@ -174,8 +174,8 @@ class ClockSampler:
         loaded = [r for r in rows if r[2] > 0.5 * max(x[2] for x in rows)] or rows
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3]) if v.lower() == "active"})
-        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(loaded)}
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_min_mhz": min(r[0] for r in loaded),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons, "samples": len(loaded)}
 
 
 # ---------------------------------------------------------------- helpers
@@ -689,7 +689,11 @@ def main():
     del ctx
     torch.cuda.empty_cache()
     if rank == 0 and world == 1 and not args.no_extra:
-        res["extra"] = run_extra(load_peaks())
+        # clocks over the whole phase: each extra measurement lasts milliseconds, below
+        # the sampler's 100 ms period
+        with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as xclocks:
+            res["extra"] = run_extra(load_peaks())
+        res["extra_clocks"] = xclocks.summary()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, sec = cpu_sample(CPU_HEADS)
         res["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": N_CORES, "kind": "oracle",
