@@ -488,17 +488,22 @@ def link_bandwidth(torch, nbytes=256 << 20, reps=5, trials=3):
     return out
 
 
-def time_calls(torch, fn, warm=3, iters=10):
+def time_calls(torch, fn, warm=3, iters=10, reps=3):
+    """ms per call: the median over `reps` timed loops of `iters` calls (CUDA
+    events), after `warm` untimed calls; one disturbed loop cannot move it."""
     for _ in range(warm):
         fn()
     torch.cuda.synchronize()
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(iters):
-        fn()
-    e.record()
-    torch.cuda.synchronize()
-    return s.elapsed_time(e) / iters
+    per_call = []
+    for _ in range(reps):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(iters):
+            fn()
+        e.record()
+        torch.cuda.synchronize()
+        per_call.append(s.elapsed_time(e) / iters)
+    return statistics.median(per_call)
 
 
 def run_extra(peaks):
