@@ -20,6 +20,9 @@
 // flash-2-3", "Using it, the real way": FlashAttention kernels handle causal masks and sliding windows
 // natively; tiles outside every row's window are never visited, the
 // block-sparse skipping that FlexAttention's block mask performs).
+// rowmax(S) comes with the TMEM load of S: the reducing form of tcgen05.ld
+// (sm_103a) returns each thread's largest value beside the values; only the
+// rows of a partly masked tile take the maximum again after masking.
 // Part of the exponentials may be evaluated on the FMA pipe as
 // 2^floor(x) * p3(x - floor(x)) with a cubic fitted in fit_exp2_poly.py: one
 // column pair in POLYK (template argument; 0 = none) goes to the cubic.
@@ -520,9 +523,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         uint32_t sr[4][32];
+        float mq[4];  // each load's maximum over its 32 columns
   #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sr[c]);
+        for (int c = 0; c < 4; ++c) tmem_ld32_max(tS + 32 * c, sr[c], mq[c]);
         tmem_ld_wait();
+        float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
         if constexpr (SEPP) {  // S is in registers: the tile's next S may be issued
           tc_fence_before();
           mbar_arrive(BAR(S_FREE + t));
@@ -533,20 +538,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         const int kv0 = 128 * j;
         if ((LEFT && kv0 < key_lo) || kv0 + 128 > key_hi) {
+          // a tile the row sees only in part: mask, then take the maximum again
+          // (eight short chains of 3-input maxima, then a small tree)
   #pragma unroll
           for (int i = 0; i < 128; ++i)
             if ((LEFT && kv0 + i < key_lo) || kv0 + i >= key_hi) x[i] = -INFINITY;
-        }
-        // row maximum: eight short chains of 3-input maxima, then a small tree
-        float mg[8];
+          float mg[8];
   #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          float m = fmaxf(x[16 * g], x[16 * g + 1]);
+          for (int g = 0; g < 8; ++g) {
+            float m = fmaxf(x[16 * g], x[16 * g + 1]);
   #pragma unroll
-          for (int i = 2; i < 16; i += 2) m = max3f(m, x[16 * g + i], x[16 * g + i + 1]);
-          mg[g] = m;
+            for (int i = 2; i < 16; i += 2) m = max3f(m, x[16 * g + i], x[16 * g + i + 1]);
+            mg[g] = m;
+          }
+          mx = max3f(max3f(mg[0], mg[1], mg[2]), max3f(mg[3], mg[4], mg[5]), fmaxf(mg[6], mg[7]));
         }
-        const float mx = max3f(max3f(mg[0], mg[1], mg[2]), max3f(mg[3], mg[4], mg[5]), fmaxf(mg[6], mg[7]));
         const float m_new = mx * sl2j;
         float alpha = 1.f;
         const bool resc = m_new > m_ref + tau;
