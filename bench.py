@@ -425,10 +425,15 @@ def run_e2e(args, ctx):
 
     run(3)
     steps = max(4, args.steps)  # the pipeline's fill and drain (one step's copies each) spread over as many steps
-    torch.cuda.synchronize()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    run(steps, start, end)
-    ms = start.elapsed_time(end) / steps
+    # the median of three timed loops: the host link is shared with the machine's other
+    # GPUs, and one loop in a run has measured half the rate of the loops around it
+    reps = []
+    for _ in range(3):
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        run(steps, start, end)
+        reps.append(start.elapsed_time(end) / steps)
+    ms = sorted(reps)[1]
     flops = F * (2.5 if have_bwd else 1.0)
     h2d = sum(t.numel() * t.element_size() for t in host_in[0].values())
     d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
@@ -438,7 +443,8 @@ def run_e2e(args, ctx):
     copy_ms = max(h2d / link["h2d_gbs"], d2h / link["d2h_gbs"], (h2d + d2h) / link["both_directions_gbs"]) * 1e-6
     return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "timing": "CUDA events joined across the three streams",
+            "timing": "CUDA events joined across the three streams; median of three timed loops",
+            "loops_ms_per_step": [round(r, 4) for r in reps],
             "pipelining": "3 streams, double-buffered device tensors",
             "link": {**link, "copy_ms_per_step": round(copy_ms, 4),
                      "copy_bound_tflops": round(flops / (copy_ms * 1e-3) / 1e12, 2)}}

@@ -221,13 +221,14 @@ static int packed_items(int num_seqs, int units_max, int total_rows, int unit) {
   return (int)items;
 }
 
-// The sliding-window kernels exist with the cubic off or on one column pair
-// in 8: a share of 1/16 maps to off, 1/4 and 1/8 to 1/8.  The e4m3 kernels
-// without a window also have 1/16 (the fastest share measured for them).
-static int window_poly(int poly) { return (poly == 4 || poly == 8) ? 8 : 0; }
+// The bf16 sliding-window kernels exist with the cubic off or on one column
+// pair in 8 or 16 (1/4 maps to 1/8).  The e4m3 kernels have 1/8 and none, and
+// without a window also 1/16 (the fastest share measured for them); with a
+// window 1/16 maps to none.
+static int window_poly(int poly) { return poly == 16 ? 16 : (poly == 4 || poly == 8) ? 8 : 0; }
 static int fp8_poly(int poly, int mask) {
-  if (mask == kMaskWindow) return window_poly(poly);
-  return poly == 16 ? 16 : window_poly(poly);
+  if (poly == 16) return mask == kMaskWindow ? 0 : 16;
+  return (poly == 4 || poly == 8) ? 8 : 0;
 }
 
 static fa_status fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu,

@@ -723,7 +723,7 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
 #define FA_FWD_CASE(DD, MM, PP) \
   if (D == DD && mask == MM && poly == PP) return launch_fwd_t<DD, MM, PP, false>(tq, tk, tv, p, grid_x, stream);
   // the cubic's share is selectable (1/4, 1/8, 1/16 of the column pairs) for
-  // the unmasked and causal kernels; the windowed ones take 1/8 or none
+  // the unmasked and causal kernels; the windowed ones take 1/8, 1/16 or none
 #define FA_FWD_CASES(DD)            \
   FA_FWD_CASE(DD, kMaskNone, 0)     \
   FA_FWD_CASE(DD, kMaskNone, 4)     \
@@ -734,7 +734,8 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   FA_FWD_CASE(DD, kMaskRight, 8)    \
   FA_FWD_CASE(DD, kMaskRight, 16)   \
   FA_FWD_CASE(DD, kMaskWindow, 0)   \
-  FA_FWD_CASE(DD, kMaskWindow, 8)
+  FA_FWD_CASE(DD, kMaskWindow, 8)   \
+  FA_FWD_CASE(DD, kMaskWindow, 16)
   FA_FWD_CASES(64)
   FA_FWD_CASES(128)
 #undef FA_FWD_CASES

@@ -475,10 +475,10 @@ fa_status fa_selftest_exp2(const float* x, float* y, int n, int which, fa_stream
  *   FA_OPT_POLY_EXP      : share of the forward's softmax exponentials
  *                          evaluated with the cubic on the FMA pipe: 0 = none
  *                          (all on the SFU), 4 / 8 / 16 = one column pair in
- *                          4 / 8 / 16 (default 16), 1 = 8 (sliding-window
- *                          kernels, bf16 or FP8: 4 and 8 mean 8, 16 means
- *                          none; other FP8 kernels: 4 means 8); other values
- *                          give FA_ERR_INVALID_ARG
+ *                          4 / 8 / 16 (default 16), 1 = 8 (bf16
+ *                          sliding-window kernels: 4 means 8; FP8 kernels:
+ *                          4 means 8, and with a window 16 means none);
+ *                          other values give FA_ERR_INVALID_ARG
  *   FA_OPT_WAIT_TIMEOUT_MS : limit of every bounded wait (default 2000)
  */
 typedef enum { FA_OPT_RESCALE_TAU = 1, FA_OPT_POLY_EXP = 2, FA_OPT_WAIT_TIMEOUT_MS = 3 } fa_option;

@@ -8,7 +8,7 @@ import torch
 
 import oracle
 import synth
-from exact_attention_94_gb300 import ops
+from exact_attention_94_gb300 import _lib, ops
 from tests.parity import assert_grad, assert_lse, assert_o
 
 pytestmark = pytest.mark.gpu
@@ -56,6 +56,23 @@ def test_masked_forward_backward(d, case):
     refs = oracle.masked_backward(f64["q"], f64["k"], f64["v"], f64["do"], scale, wl, wr)
     for name, ref in zip(("dq", "dk", "dv"), refs):
         assert_grad(synth.to_f64(r[name]), ref, f"{name} {tag}")
+
+
+@pytest.mark.parametrize("poly", [0, 4, 8, 16])
+@pytest.mark.parametrize("d", [64, 128])
+def test_window_forward_cubic_share(d, poly):
+    """The sliding-window kernels at each share of exponentials on the cubic
+    (one column pair in 8 or 16, or none; 1/4 runs as 1/8)."""
+    x = synth.make_masked(2, 777, 777, 4, 2, d, seed=31 + d + poly)
+    ops.set_option(_lib.FA_OPT_POLY_EXP, poly)
+    try:
+        r = _run(x, d, 100, 0, grads=False)
+    finally:
+        ops.set_option(_lib.FA_OPT_POLY_EXP, _lib.FA_POLY_EXP_DEFAULT)
+    f64 = {n: synth.to_f64(x[n]) for n in x}
+    o_ref, l_ref = oracle.masked_forward(f64["q"], f64["k"], f64["v"], 1.0 / math.sqrt(d), 100, 0)
+    assert_o(synth.to_f64(r["o"]), o_ref, f"O window d{d} cubic 1/{poly}")
+    assert_lse(r["lse"].cpu().numpy(), l_ref, f"lse window d{d} cubic 1/{poly}")
 
 
 def test_rows_without_keys_and_unseen_keys():
