@@ -285,11 +285,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_S = [&](int t, int slot) {
         const uint32_t qa = q_s + t * TILE, ka = kv_s + slot * TILE;
         const uint32_t dst = t ? tS1 : tS0;
+        // e4m3: descriptors built once and advanced by an add (measured 1.4% faster there;
+        // no difference for bf16)
+        [[maybe_unused]] const uint64_t qd = smem_desc_sw128(qa, 16, 1024), kd = smem_desc_sw128(ka, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < (int)(D * L::kElt / 32); ++kk) {
           const uint32_t off = (kk / 4) * CHUNK + (kk % 4) * 32;
           if constexpr (F8)
-            mma_ss_f8_w(dst, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024), IDESC_S, kk > 0);
+            mma_ss_f8_w(dst, desc_add(qd, off), desc_add(kd, off), IDESC_S, kk > 0);
           else
             mma_ss_w(dst, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024), IDESC_S, kk > 0);
         }
@@ -301,9 +304,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t dst = t ? tO1 : tO0;
         const uint32_t pa = SEPP ? tmem + 384u + 64u * t : (t ? tS1 : tS0);
         if constexpr (F8) {
+          const uint64_t vd = smem_desc_sw128(va, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts_f8_w(dst, pa + kk * 8, smem_desc_sw128(va + kk * 32, 16, 1024), IDESC_O, (acc || kk > 0) ? 1u : 0u);
+            mma_ts_f8_w(dst, pa + kk * 8, desc_add(vd, kk * 32), IDESC_O, (acc || kk > 0) ? 1u : 0u);
         } else {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
