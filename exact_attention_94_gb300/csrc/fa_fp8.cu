@@ -31,17 +31,26 @@ constexpr int kRowsPerWarp = kQuantThreads == 512 ? 8 : 16;
 constexpr int kElems = 16;          // consecutive elements per lane
 
 // Butterflies of widths 1 .. 8 inside the lane's 16 elements, then widths
-// 16 * hl with the lane that differs in bit hl (hl < lanes per row).
+// 16 * hl with the lane that differs in bit hl (hl < lanes per row).  The
+// elements are held as eight fp32 pairs: width 1 pairs the two halves of a
+// pair (scalar), widths 2 .. 8 and the cross-lane stages use the packed
+// f32x2 add, subtract and FMA, which round exactly like the scalar ones.
 template <int LPR>
-__device__ __forceinline__ void fwht_row16(float (&v)[kElems], int lane) {
+__device__ __forceinline__ void fwht_row16(uint64_t (&vp)[kElems / 2], int lane) {
 #pragma unroll
-  for (int h = 1; h < kElems; h <<= 1) {
+  for (int i = 0; i < kElems / 2; ++i) {
+    float a, b;
+    f2_unpack(vp[i], a, b);
+    vp[i] = f2_pack(a + b, a - b);
+  }
 #pragma unroll
-    for (int i = 0; i < kElems; ++i) {
+  for (int h = 1; h < kElems / 2; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < kElems / 2; ++i) {
       if (!(i & h)) {
-        const float a = v[i], b = v[i + h];
-        v[i] = a + b;
-        v[i + h] = a - b;
+        const uint64_t a = vp[i], b = vp[i + h];
+        vp[i] = f2_add(a, b);
+        vp[i + h] = f2_sub(a, b);
       }
     }
   }
@@ -50,10 +59,14 @@ __device__ __forceinline__ void fwht_row16(float (&v)[kElems], int lane) {
 #pragma unroll
   for (int hl = 1; hl < LPR; hl <<= 1) {
     const float sg = (lane & hl) ? -1.f : 1.f;
+    const uint64_t sg2 = f2_pack(sg, sg);
 #pragma unroll
-    for (int i = 0; i < kElems; ++i) {
-      const float o = __shfl_xor_sync(0xffffffffu, v[i], hl);
-      v[i] = fmaf(v[i], sg, o);
+    for (int i = 0; i < kElems / 2; ++i) {
+      float lo, hi;
+      f2_unpack(vp[i], lo, hi);
+      lo = __shfl_xor_sync(0xffffffffu, lo, hl);
+      hi = __shfl_xor_sync(0xffffffffu, hi, hl);
+      vp[i] = f2_fma(vp[i], sg2, f2_pack(lo, hi));
     }
   }
 }
@@ -82,7 +95,7 @@ __global__ void __launch_bounds__(kQuantThreads) fa_fp8_quant_kernel(const __nv_
     for (int e = 0; e < kElems; ++e) neg |= (signs[seg * kElems + e] < 0 ? 1u : 0u) << e;
   }
 
-  float v[IT][kElems];
+  uint64_t v[IT][kElems / 2];  // pairs of fp32 elements
   float amax = 0.f;
 #pragma unroll
   for (int it = 0; it < IT; ++it) {
@@ -92,18 +105,18 @@ __global__ void __launch_bounds__(kQuantThreads) fa_fp8_quant_kernel(const __nv_
       const uint4 w0 = src[0], w1 = src[1];
       const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[i]));
-        v[it][2 * i] = f.x;
-        v[it][2 * i + 1] = f.y;
-      }
+      for (int i = 0; i < 8; ++i) v[it][i] = f2_pack(__uint_as_float(wv[i] << 16), __uint_as_float(wv[i] & 0xffff0000u));
     } else {
 #pragma unroll
-      for (int e = 0; e < kElems; ++e) v[it][e] = 0.f;
+      for (int i = 0; i < kElems / 2; ++i) v[it][i] = 0ull;
     }
     if (ROT) fwht_row16<LPR>(v[it], lane);  // the signs come with the scale below
 #pragma unroll
-    for (int e = 0; e < kElems; e += 2) amax = max3f(amax, fabsf(v[it][e]), fabsf(v[it][e + 1]));
+    for (int i = 0; i < kElems / 2; ++i) {
+      float a, b;
+      f2_unpack(v[it][i], a, b);
+      amax = max3f(amax, fabsf(a), fabsf(b));
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -117,9 +130,10 @@ __global__ void __launch_bounds__(kQuantThreads) fa_fp8_quant_kernel(const __nv_
   if (threadIdx.x == 0) scales[((size_t)b * H + h) * nblk + blk] = scale;
   // x * sign * (1 / scale) as x * (sign * (1 / scale)): the sign is exact and
   // round-to-nearest is symmetric, so each code (and each zero's sign) is the same
-  float sinv[kElems];
+  uint64_t sinv[kElems / 2];
 #pragma unroll
-  for (int e = 0; e < kElems; ++e) sinv[e] = ((neg >> e) & 1u) ? -inv : inv;
+  for (int i = 0; i < kElems / 2; ++i)
+    sinv[i] = f2_pack(((neg >> (2 * i)) & 1u) ? -inv : inv, ((neg >> (2 * i + 1)) & 1u) ? -inv : inv);
 
 #pragma unroll
   for (int it = 0; it < IT; ++it) {
@@ -127,9 +141,12 @@ __global__ void __launch_bounds__(kQuantThreads) fa_fp8_quant_kernel(const __nv_
     const int n = blk * 128 + rr;
     uint32_t wd[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      wd[q] = pack_e4m3x4(__fmul_rn(v[it][4 * q], sinv[4 * q]), __fmul_rn(v[it][4 * q + 1], sinv[4 * q + 1]),
-                          __fmul_rn(v[it][4 * q + 2], sinv[4 * q + 2]), __fmul_rn(v[it][4 * q + 3], sinv[4 * q + 3]));
+    for (int q = 0; q < 4; ++q) {
+      float y0, y1, y2, y3;
+      f2_unpack(f2_mul(v[it][2 * q], sinv[2 * q]), y0, y1);
+      f2_unpack(f2_mul(v[it][2 * q + 1], sinv[2 * q + 1]), y2, y3);
+      wd[q] = pack_e4m3x4(y0, y1, y2, y3);
+    }
     uint4 word = make_uint4(wd[0], wd[1], wd[2], wd[3]);
     if (!(amax > 0.f)) word = make_uint4(0u, 0u, 0u, 0u);  // all-zero block: +0 codes (not -0 from flipped zeros)
     if constexpr (TR) {
