@@ -520,6 +520,25 @@ def run_extra(peaks):
     from exact_attention_94_gb300 import _lib, accounting as acc, ops
 
     out = {}
+    # fp8 first, before seconds of load bring the power cap in (the e4m3 products draw the
+    # most power): the long workload's shape on e4m3 operands (quantise Q, K with the
+    # Hadamard rotation and V transposed, then attend), causal
+    w = synth.WORKLOADS["long"]
+    x = synth.make_dense(w.B, w.H, w.N, w.d, seed=w.seed, k_boost=w.k_boost, device="cuda", with_do=False)
+    signs = synth.hadamard_signs(w.d, 0).cuda()
+    F = acc.fwd_flops(w.B, w.H, w.N, w.d, True)
+    qc, qs = ops.fp8_quantize(x["q"], signs)
+    kc, ks = ops.fp8_quantize(x["k"], signs)
+    vc, vs = ops.fp8_quantize(x["v"], None, transpose=True)
+    t_att = time_calls(torch, lambda: ops.fwd_fp8_codes(qc, kc, vc, qs, ks, vs, causal=True), warm=3, iters=20)
+    t_all = time_calls(torch, lambda: ops.fwd_fp8(x["q"], x["k"], x["v"], signs, causal=True), warm=3, iters=20)
+    fp8_peak = 2.0 * peaks["bf16_tflops"]  # measured bf16 burst x the nominal e4m3 / bf16 ratio of 2
+    out["fp8"] = {"attn_ms": round(t_att, 4), "attn_tflops": round(F / t_att / 1e9, 1),
+                  "attn_frac_of_fp8_peak": round(F / t_att / 1e9 / fp8_peak, 4),
+                  "with_quantize_ms": round(t_all, 4), "with_quantize_tflops": round(F / t_all / 1e9, 1),
+                  "fp8_peak_tflops": fp8_peak, "peak_source": "measured bf16 burst x 2 (nominal ratio)"}
+    del x, qc, kc, vc
+    torch.cuda.empty_cache()
     # mid: B16 H16 N2048 d64 non-causal
     w = synth.WORKLOADS["mid"]
     x = synth.make_dense(w.B, w.H, w.N, w.d, seed=0, device="cuda")
@@ -571,24 +590,6 @@ def run_extra(peaks):
     out["prefill"] = {"fwd_ms": round(t_f, 4), "fwd_tflops": round(F / t_f / 1e9, 1),
                       "flops": "visible scores only, 4d per score"}
     del x
-    torch.cuda.empty_cache()
-    # fp8: the long workload's shape on e4m3 operands (quantise Q, K with the
-    # Hadamard rotation and V transposed, then attend), causal
-    w = synth.WORKLOADS["long"]
-    x = synth.make_dense(w.B, w.H, w.N, w.d, seed=w.seed, k_boost=w.k_boost, device="cuda", with_do=False)
-    signs = synth.hadamard_signs(w.d, 0).cuda()
-    F = acc.fwd_flops(w.B, w.H, w.N, w.d, True)
-    qc, qs = ops.fp8_quantize(x["q"], signs)
-    kc, ks = ops.fp8_quantize(x["k"], signs)
-    vc, vs = ops.fp8_quantize(x["v"], None, transpose=True)
-    t_att = time_calls(torch, lambda: ops.fwd_fp8_codes(qc, kc, vc, qs, ks, vs, causal=True), warm=3, iters=20)
-    t_all = time_calls(torch, lambda: ops.fwd_fp8(x["q"], x["k"], x["v"], signs, causal=True), warm=3, iters=20)
-    fp8_peak = 2.0 * peaks["bf16_tflops"]  # measured bf16 burst x the nominal e4m3 / bf16 ratio of 2
-    out["fp8"] = {"attn_ms": round(t_att, 4), "attn_tflops": round(F / t_att / 1e9, 1),
-                  "attn_frac_of_fp8_peak": round(F / t_att / 1e9 / fp8_peak, 4),
-                  "with_quantize_ms": round(t_all, 4), "with_quantize_tflops": round(F / t_all / 1e9, 1),
-                  "fp8_peak_tflops": fp8_peak, "peak_source": "measured bf16 burst x 2 (nominal ratio)"}
-    del x, qc, kc, vc
     torch.cuda.empty_cache()
     # decode: B64 L32768 H32 d128 (34.4 GB of K/V, far larger than L2)
     w = synth.WORKLOADS["decode"]
